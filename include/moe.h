@@ -1,0 +1,222 @@
+/*
+ * moe.h -- C ABI of the single-GPU MoE-layer forward for GB300 (sm_103a).
+ *
+ * The operation (from "Mixture-of-Kittens: MoE Megakernel for NVL72s",
+ * Sec. 2.1, Eq. "MoE", and the vendor blog's E_i(x) with SiLU):
+ *
+ *   MoE(x) = f_shared(x) + sum_{i in E(x)} g_i f_i(x),   g_i = s_i / sum_{j in E(x)} s_j,
+ *   f_i(x) = W_down^(i) ( SiLU(W_gate^(i) x) * W_up^(i) x ),
+ *
+ * E(x) = the k routed experts with the highest router score s = score(W_r x + b)
+ * (score = sigmoid, or softmax over all experts).  All experts are on this GPU:
+ * the paper's cross-GPU dispatch/combine become an on-device gather into a
+ * fixed-size ring of minibatches and a scatter back to token order.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers on the plan's device;
+ *     the caller owns all memory (inputs, outputs, workspace) and the stream.
+ *   - Matrices are row-major; every weight is K-major (its contraction
+ *     dimension contiguous), exactly the shapes of Sec. 2.1: W_up, W_gate in
+ *     R^{I x D}, W_down in R^{D x I}; expert e's matrix is block e of the
+ *     stacked [E, ...] array.
+ *   - bf16 = IEEE bfloat16 bit patterns (2 bytes).
+ *   - Calls are asynchronous on `stream`, allocate nothing on the device, do
+ *     not synchronise the host, and never read device memory on the host;
+ *     device-side failures are reported through moe_get_status().
+ *   - Return value: MOE_OK (0) or a negative moe_error; no C++ exception
+ *     crosses this interface.
+ *   - Plans are immutable after creation and may be shared by threads; one
+ *     workspace must not be used by two forwards that overlap on the GPU.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum moe_error {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* null pointer, T > T_max, bad enum value */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* shape outside the limits listed at moe_config */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+  MOE_ERR_CUDA = -4,               /* a CUDA runtime call failed (launch, copy, attribute) */
+  MOE_ERR_UNSUPPORTED_DEVICE = -5  /* the current device is not sm_103 */
+} moe_error;
+
+typedef enum moe_device_status {
+  MOE_STATUS_OK = 0,
+  MOE_STATUS_TIMEOUT = 1,          /* a device-side wait exceeded its limit; outputs are invalid */
+  MOE_STATUS_SCHEDULE_INVALID = 2  /* an expert index out of range or route counts inconsistent */
+} moe_device_status;
+
+typedef enum moe_score_fn { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_fn;
+typedef enum moe_precision { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precision;
+
+/*
+ * Layer shape and execution knobs.
+ *   T_max  largest token count a forward will be called with (>= 1)
+ *   D      hidden size, multiple of 256
+ *   I      routed-expert intermediate size, multiple of 128
+ *   E      routed experts, 1..512
+ *   k      experts per token, 1..min(16, E)
+ *   I_s    shared-expert intermediate size, multiple of 128, or 0 (no shared expert)
+ *   score_fn   moe_score_fn
+ *   precision  moe_precision of the routed experts (the router and the shared
+ *              expert always run in bf16, Sec. 3.4 "MXFP8 Support")
+ *   minibatch  b: routes per minibatch of the dispatch ring, multiple of 128,
+ *              128..32768 (Sec. 3.2 sweeps 512..32768)
+ *   ring_slots minibatch slots in the ring (>= lag + 1); ring_slots * minibatch
+ *              >= T*k gives the over-allocated (no wrap) buffer of Sec. 3.3
+ *   gather_ctas  CTAs (one per SM) that only gather tokens, >= 1 (Sec. 3.4
+ *              "Computation-Communication SM Tuning")
+ *   gemm_ctas  CTAs that run expert GEMMs; 0 = all remaining SMs
+ *   lag        0: down projections of minibatch m follow its up/gate tiles;
+ *              1: they follow the up/gate tiles of minibatch m + 1
+ *   timeout_ms limit of every device-side wait (0 = 2000 ms)
+ * Zero for minibatch / ring_slots / gather_ctas / lag picks the defaults
+ * (8192 / 4 / 8 / 1).
+ */
+typedef struct moe_config {
+  int64_t T_max;
+  int64_t D;
+  int64_t I;
+  int64_t E;
+  int64_t k;
+  int64_t I_s;
+  int32_t score_fn;
+  int32_t precision;
+  int32_t minibatch;
+  int32_t ring_slots;
+  int32_t gather_ctas;
+  int32_t gemm_ctas;
+  int32_t lag;
+  int32_t timeout_ms;
+  int32_t reserved[4];
+} moe_config;
+
+/*
+ * Layer parameters (device pointers).
+ *   W_router [E, D] bf16;  b_router [E] fp32 or NULL (no bias; the bias is
+ *   added to the logits before the score function)
+ *   bf16 precision:  W_up, W_gate [E, I, D] bf16;  W_down [E, D, I] bf16;
+ *                    the *_scale pointers are ignored
+ *   MXFP8 precision: W_up, W_gate [E, I, D] and W_down [E, D, I] E4M3 codes
+ *                    (1 byte), and *_scale the E8M0 block scales written by
+ *                    moe_quantize_mxfp8 for the same matrices
+ *   Ws_up, Ws_gate [I_s, D] bf16; Ws_down [D, I_s] bf16; all three NULL = no
+ *   shared expert in this call (required when I_s = 0)
+ */
+typedef struct moe_weights {
+  const void* W_router;
+  const float* b_router;
+  const void* W_up;
+  const void* W_gate;
+  const void* W_down;
+  const uint8_t* W_up_scale;
+  const uint8_t* W_gate_scale;
+  const uint8_t* W_down_scale;
+  const void* Ws_up;
+  const void* Ws_gate;
+  const void* Ws_down;
+} moe_weights;
+
+/*
+ * Outputs (device pointers).  `out` is required; every other field may be
+ * NULL (not exported).
+ *   out            [T, D] bf16: MoE(x)
+ *   topk_idx       [T, k] int32: selected experts, ascending id per token
+ *   topk_w         [T, k] fp32: g, same order
+ *   expert_counts  [E] int32: M_e, routes per expert (Algorithm 1)
+ *   expert_offsets [E + 1] int32: S_e, exclusive prefix of M (S_E = T*k)
+ *   sched          [T*k, 3] int32: schedule table row P = {src_index t,
+ *                  expert e, dst_index j = t*k + slot}, rows sorted by expert
+ *                  then token (Algorithm 1 with one rank)
+ *   route_row      [T*k] int32: inverse of sched, route j -> row P
+ */
+typedef struct moe_outputs {
+  void* out;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* expert_counts;
+  int32_t* expert_offsets;
+  int32_t* sched;
+  int32_t* route_row;
+} moe_outputs;
+
+typedef struct moe_plan moe_plan;
+
+/*
+ * Validate `cfg` for the current CUDA device and create a plan.
+ * Errors: MOE_ERR_INVALID_ARG (null), MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_UNSUPPORTED_DEVICE, MOE_ERR_CUDA.  *out is NULL on failure.
+ * Host memory only; the caller releases it with moe_plan_destroy.
+ */
+int moe_plan_create(const moe_config* cfg, moe_plan** out);
+
+/* Release a plan (NULL is accepted).  Returns MOE_OK. */
+int moe_plan_destroy(moe_plan* plan);
+
+/* Bytes of device workspace a forward of T tokens needs (0 on bad input).
+ * The workspace holds the routing results, the schedule, the task list, the
+ * dispatch ring, the gated activations and the token-order staging rows. */
+size_t moe_workspace_bytes(const moe_plan* plan, int64_t T);
+
+/*
+ * MXFP8 weight pre-quantisation (Sec. 3.4 "MXFP8 Support", OCP MX v1.0):
+ * W [rows, K] bf16 (device), K multiple of 32 -> q [rows, K] E4M3 codes and
+ * scales (E8M0, one per 32 consecutive K elements) in the library's layout,
+ * moe_mxfp8_scale_bytes(rows, K) bytes.  Block scale X = 2^(floor(log2 amax)
+ * - 8), elements rounded to nearest-even and saturated at +-448; an all-zero
+ * block gets X = 2^-127.  Asynchronous on `stream`.
+ */
+int moe_quantize_mxfp8(const moe_plan* plan, const void* W, int64_t rows, int64_t K, uint8_t* q,
+                       uint8_t* scales, moe_stream_t stream);
+size_t moe_mxfp8_scale_bytes(int64_t rows, int64_t K);
+
+/*
+ * The forward pass for T tokens (0 <= T <= T_max; T = 0 does nothing).
+ *   x          [T, D] bf16 (device)
+ *   w          layer parameters, see moe_weights
+ *   o          outputs, see moe_outputs
+ *   workspace  device memory of at least moe_workspace_bytes(plan, T) bytes,
+ *              256-byte aligned; its contents need no initialisation
+ * Launches, in order on `stream`: router + top-k, schedule, persistent
+ * forward kernel; with no host synchronisation.  Two calls on identical
+ * inputs give bitwise-identical outputs, also across minibatch, ring_slots,
+ * gather_ctas, gemm_ctas and lag settings.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA.
+ */
+int moe_fwd(const moe_plan* plan, int64_t T, const void* x, const moe_weights* w, const moe_outputs* o,
+            void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Read the device status word of the last forward that used `workspace`
+ * (a moe_device_status).  This call waits for `stream` to finish: it is the
+ * one host synchronisation point, taken only when the caller asks.
+ */
+int moe_get_status(const moe_plan* plan, const void* workspace, int* device_status, moe_stream_t stream);
+
+/*
+ * Optional per-launch timing for profiling harnesses: with events != NULL,
+ * every later moe_fwd with this plan records events[0] (cudaEvent_t) on its
+ * stream before the router launch, events[1] after it, events[2] after the
+ * schedule launch and events[3] after the persistent kernel; events == NULL
+ * turns it off.  The caller owns the events.  Not to be called while another
+ * thread runs moe_fwd with the same plan.
+ */
+int moe_plan_set_timing_events(moe_plan* plan, void* const* events);
+
+/* Static description of an error code. */
+const char* moe_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

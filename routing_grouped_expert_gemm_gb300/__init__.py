@@ -1,0 +1,199 @@
+"""Python binding of the MoE-layer forward C ABI (``include/moe.h``).
+
+Argument marshalling only: every step of the forward runs in the CUDA library
+``_lib/libmoe_gb300.so`` (built by ``build.py``).  There is no fallback: if the
+library is missing or cannot be loaded, every entry point raises.  PyTorch is
+used only to hand over device pointers and streams.
+
+Entry points keep the C names: ``moe_plan_create``, ``moe_plan_destroy``,
+``moe_workspace_bytes``, ``moe_quantize_mxfp8``, ``moe_mxfp8_scale_bytes``,
+``moe_fwd``, ``moe_get_status``, ``moe_error_string``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED_SHAPE = -2
+MOE_ERR_WORKSPACE_TOO_SMALL = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_UNSUPPORTED_DEVICE = -5
+MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID = 0, 1, 2
+MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
+MOE_PREC_BF16, MOE_PREC_MXFP8 = 0, 1
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {moe_error_string(code)} ({code})")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T_max", ctypes.c_int64), ("D", ctypes.c_int64), ("I", ctypes.c_int64), ("E", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("I_s", ctypes.c_int64), ("score_fn", ctypes.c_int32),
+                ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
+                ("gather_ctas", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32), ("lag", ctypes.c_int32),
+                ("timeout_ms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "W_router", "b_router", "W_up", "W_gate", "W_down", "W_up_scale", "W_gate_scale", "W_down_scale",
+        "Ws_up", "Ws_gate", "Ws_down")]
+
+
+class moe_outputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "out", "topk_idx", "topk_w", "expert_counts", "expert_offsets", "sched", "route_row")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run routing_grouped_expert_gemm_gb300/build.py)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, sz, i32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int)
+    L.moe_plan_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(vp)]
+    L.moe_plan_create.restype = ctypes.c_int
+    L.moe_plan_destroy.argtypes = [vp]
+    L.moe_plan_destroy.restype = ctypes.c_int
+    L.moe_workspace_bytes.argtypes = [vp, i64]
+    L.moe_workspace_bytes.restype = sz
+    L.moe_quantize_mxfp8.argtypes = [vp, vp, i64, i64, vp, vp, vp]
+    L.moe_quantize_mxfp8.restype = ctypes.c_int
+    L.moe_mxfp8_scale_bytes.argtypes = [i64, i64]
+    L.moe_mxfp8_scale_bytes.restype = sz
+    L.moe_fwd.argtypes = [vp, i64, vp, ctypes.POINTER(moe_weights), ctypes.POINTER(moe_outputs), vp, sz, vp]
+    L.moe_fwd.restype = ctypes.c_int
+    L.moe_get_status.argtypes = [vp, vp, i32p, vp]
+    L.moe_get_status.restype = ctypes.c_int
+    L.moe_plan_set_timing_events.argtypes = [vp, ctypes.POINTER(vp)]
+    L.moe_plan_set_timing_events.restype = ctypes.c_int
+    L.moe_error_string.argtypes = [ctypes.c_int]
+    L.moe_error_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def declared_functions() -> list[str]:
+    """Function names declared in include/moe.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def _ptr(v) -> int | None:
+    if v is None:
+        return None
+    if isinstance(v, int):
+        return v
+    return int(v.data_ptr())  # torch tensor
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def moe_error_string(code: int) -> str:
+    return lib().moe_error_string(code).decode()
+
+
+class Plan:
+    """Owns a moe_plan*; released by moe_plan_destroy (or garbage collection)."""
+
+    def __init__(self, handle: int, cfg: moe_config):
+        self.handle = handle
+        self.cfg = cfg
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.moe_plan_destroy(self.handle)
+            self.handle = None
+
+
+def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
+                    ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0) -> Plan:
+    if isinstance(score_fn, str):
+        score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
+    if isinstance(precision, str):
+        precision = {"bf16": MOE_PREC_BF16, "mxfp8": MOE_PREC_MXFP8}[precision]
+    cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
+                     lag, timeout_ms)
+    h = ctypes.c_void_p()
+    rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_plan_create")
+    return Plan(h.value, cfg)
+
+
+def moe_plan_destroy(plan: Plan) -> None:
+    if plan.handle:
+        lib().moe_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+def moe_workspace_bytes(plan: Plan, T: int) -> int:
+    return int(lib().moe_workspace_bytes(plan.handle, T))
+
+
+def moe_mxfp8_scale_bytes(rows: int, K: int) -> int:
+    return int(lib().moe_mxfp8_scale_bytes(rows, K))
+
+
+def moe_quantize_mxfp8(plan: Plan, W, rows: int, K: int, q, scales, stream=None) -> None:
+    rc = lib().moe_quantize_mxfp8(plan.handle, _ptr(W), rows, K, _ptr(q), _ptr(scales), _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_quantize_mxfp8")
+
+
+def moe_fwd(plan: Plan, T: int, x, weights: dict, out, workspace, workspace_bytes: int | None = None,
+            topk_idx=None, topk_w=None, expert_counts=None, expert_offsets=None, sched=None, route_row=None,
+            stream=None) -> None:
+    """weights: dict with keys of moe_weights (W_router, b_router, W_up, ...)."""
+    w = moe_weights(**{k: _ptr(v) for k, v in weights.items()})
+    o = moe_outputs(_ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts), _ptr(expert_offsets),
+                    _ptr(sched), _ptr(route_row))
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().moe_fwd(plan.handle, T, _ptr(x), ctypes.byref(w), ctypes.byref(o), _ptr(workspace),
+                       workspace_bytes, _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_fwd")
+
+
+def moe_get_status(plan: Plan, workspace, stream=None) -> int:
+    st = ctypes.c_int(-1)
+    rc = lib().moe_get_status(plan.handle, _ptr(workspace), ctypes.byref(st), _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_get_status")
+    return st.value
+
+
+def moe_plan_set_timing_events(plan: Plan, events) -> None:
+    """events: four torch.cuda.Event (created with enable_timing) or None."""
+    if events is None:
+        rc = lib().moe_plan_set_timing_events(plan.handle, None)
+    else:
+        arr = (ctypes.c_void_p * 4)(*[int(e.cuda_event) for e in events])
+        rc = lib().moe_plan_set_timing_events(plan.handle, arr)
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_plan_set_timing_events")

@@ -1,0 +1,171 @@
+// Shared definitions of the MoE forward kernels: launch parameters, the task
+// record the schedule kernel writes for the persistent kernel, workspace
+// sections and bounded device-side waits.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace moe {
+
+typedef __nv_bfloat16 bf16;
+
+// GEMM tiling shared by all tcgen05 kernels
+constexpr int BM = 128;          // rows (tokens) per tile = UMMA M
+constexpr int BK = 64;           // K per stage = one 128-byte swizzle atom of bf16
+constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
+constexpr int BN_UP = 128;       // intermediate columns per GEMM1 tile (x2: up and gate)
+constexpr int BN_DOWN = 256;     // output columns per GEMM2 tile
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_STAGE_BYTES = 256 * BK * 2;       // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int ACC_COLS = 256;    // fp32 accumulator columns per tile
+constexpr int MEGA_THREADS = 256;  // 8 warps
+constexpr int ROUTER_THREADS = 192;
+constexpr int SCHED_THREADS = 512;
+constexpr int TOPK_MAX = 16;
+constexpr int E_MAX = 512;
+
+// device status codes (written to the workspace status word)
+enum : int { STATUS_OK = 0, STATUS_TIMEOUT = 1, STATUS_SCHEDULE_INVALID = 2 };
+
+// task kinds of the persistent kernel
+enum : int { TASK_R1 = 0, TASK_R2 = 1, TASK_S1 = 2, TASK_S2 = 3 };
+
+struct Task {      // 64 bytes
+  int kind;        // TASK_*
+  int n;           // output column tile
+  int e;           // routed expert (0 for the shared expert)
+  int a_row;       // row coordinate of the A operand in its tensor map
+  int rows;        // valid rows of the tile (<= BM)
+  int p0;          // first schedule row (routed) / first token (shared)
+  int out_row;     // first output row (R1: ring_h row, S1/S2: token)
+  int dep0, need0; // wait until counters[dep0] >= need0 (dep < 0: none)
+  int dep1, need1;
+  int done0, done1;  // counters incremented when the tile is stored (-1: none)
+  int pad[3];
+};
+static_assert(sizeof(Task) == 64, "task record is 64 bytes");
+
+// meta block written by the schedule kernel (int32 offsets)
+enum : int { META_N_TASKS = 0, META_N_MTILES = 1, META_TOTAL_Y = 2 /* R2 tasks */, META_MB = 4 };
+// META_MB + 2*m: R1 task count of minibatch m; META_MB + 2*m + 1: R2 task count
+
+struct FwdParams {
+  int T, D, I, E, k, I_s;
+  int score_fn;
+  int b, slots, G, n_gemm, lag;
+  int n_mb, R;          // minibatches, routes (T*k)
+  int N1, N2, N1s, N2s; // column tiles: I/128, D/256, I_s/128, D/256
+  int n_chunks;         // router tiles = ceil(T/128)
+  int n_router_cols;    // E rounded up (MMA N of the router)
+  int n_mtiles_max, n_smtiles, n_tasks_max;
+  int n_counters;
+  long long timeout_ns;
+  // inputs
+  const bf16* x;
+  const float* b_router;
+  // workspace sections
+  int* status;
+  int* counters;      // zeroed by the router kernel
+  int* meta;
+  int* topk_idx;      // [T,k]
+  float* topk_w;      // [T,k]
+  int* chunk_counts;  // [n_chunks, E]
+  int* M;             // [E]
+  int* S;             // [E+1]
+  int* sched;         // [R,3] {src_index t, expert e, dst_index j}
+  int* route_row;     // [R]
+  int* mtiles;        // [n_mtiles_max, 4] {e, p0, rows, m}
+  int* segs;          // scratch for the task builder
+  Task* tasks;        // [n_tasks_max]
+  bf16* ring_x;       // [slots*b, D]
+  bf16* ring_h;       // [slots*b, I]
+  bf16* h_s;          // [T, I_s]
+  float* Y;           // [R, D] fp32, token order (row j = t*k + slot)
+  bf16* out;          // [T, D]
+};
+
+// counter indices
+__host__ __device__ inline int ctr_ydone() { return 0; }
+__host__ __device__ inline int ctr_filled(const FwdParams& p, int m) { return 1 + m; }
+__host__ __device__ inline int ctr_r1(const FwdParams& p, int m) { return 1 + p.n_mb + m; }
+__host__ __device__ inline int ctr_r2(const FwdParams& p, int m) { return 1 + 2 * p.n_mb + m; }
+__host__ __device__ inline int ctr_hready(const FwdParams& p, int mt) { return 1 + 3 * p.n_mb + mt; }
+__host__ __device__ inline int ctr_shready(const FwdParams& p, int mt) {
+  return 1 + 3 * p.n_mb + p.n_mtiles_max + mt;
+}
+__host__ __device__ inline int n_counters(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
+
+struct TensorMaps {
+  CUtensorMap x;        // [T, D]            box {64, 128}
+  CUtensorMap ring_x;   // [slots*b, D]      box {64, 128}
+  CUtensorMap w_up;     // [E*I, D]          box {64, 128}
+  CUtensorMap w_gate;   // [E*I, D]          box {64, 128}
+  CUtensorMap ring_h;   // [slots*b, I]      box {64, 128}
+  CUtensorMap w_down;   // [E*D, I]          box {64, 256}
+  CUtensorMap ws_up;    // [I_s, D]          box {64, 128}
+  CUtensorMap ws_gate;  // [I_s, D]          box {64, 128}
+  CUtensorMap h_s;      // [T, I_s]          box {64, 128}
+  CUtensorMap ws_down;  // [D, I_s]          box {64, 256}
+};
+
+struct RouterMaps {
+  CUtensorMap x;   // [T, D] box {64, 128}
+  CUtensorMap wr;  // [E, D] box {64, n_router_cols} (or half of it when E > 256)
+};
+
+// ------------------------------------------------------------------ bounded waits
+// Every wait gives up after timeout_ns (or as soon as another thread has set a
+// non-zero status), records STATUS_TIMEOUT and returns false; callers then
+// stop issuing work and leave cleanly.
+__device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ bool wait_counter_ge(const int* ctr, int need, int* status, long long timeout_ns) {
+  if (ld_acquire_gpu(ctr) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (ld_acquire_gpu(ctr) >= need) return true;
+    if ((++it & 31u) == 0) {
+      if (ld_relaxed_gpu(status) != 0) return false;
+      if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) {
+        raise_status(status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++it & 63u) == 0) {
+      if (ld_relaxed_gpu(status) != 0) return false;
+      if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) {
+        raise_status(status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + __expf(-v)); }
+
+}  // namespace moe

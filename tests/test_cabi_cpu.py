@@ -1,0 +1,75 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/moe.h declares, and validates arguments on the host."""
+import ctypes
+import subprocess
+
+import pytest
+import torch
+
+import routing_grouped_expert_gemm_gb300 as rg
+from routing_grouped_expert_gemm_gb300 import build as rgbuild
+
+
+@pytest.fixture(scope="module")
+def L():
+    rgbuild.build()
+    return rg.lib()
+
+
+EXPECTED = {"moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_quantize_mxfp8",
+            "moe_mxfp8_scale_bytes", "moe_fwd", "moe_get_status", "moe_error_string",
+            "moe_plan_set_timing_events"}
+
+
+def test_header_declares_the_boundary():
+    assert EXPECTED <= set(rg.declared_functions())
+
+
+def test_library_exports_every_declared_function(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", rg.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in rg.declared_functions():
+        assert name in exported, name
+        assert getattr(L, name) is not None
+
+
+def test_error_strings(L):
+    assert rg.moe_error_string(0) == "ok"
+    assert "workspace" in rg.moe_error_string(rg.MOE_ERR_WORKSPACE_TOO_SMALL)
+    assert rg.moe_error_string(123) == "unknown error"
+
+
+@pytest.mark.parametrize("kw", [
+    dict(D=100), dict(D=384), dict(I=96), dict(E=0), dict(E=513), dict(k=0), dict(k=17), dict(k=9, E=8),
+    dict(I_s=100), dict(minibatch=100), dict(minibatch=65536), dict(ring_slots=1, lag=1),
+])
+def test_plan_rejects_unsupported_shapes(L, kw):
+    base = dict(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
+    base.update(kw)
+    with pytest.raises(rg.MoEError) as ei:
+        rg.moe_plan_create(**base)
+    assert ei.value.code == rg.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_plan_rejects_bad_enums(L):
+    for kw in (dict(score_fn=7), dict(precision=9), dict(lag=3)):
+        with pytest.raises(rg.MoEError) as ei:
+            rg.moe_plan_create(T_max=256, D=256, I=128, E=16, k=4, **kw)
+        assert ei.value.code == rg.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_plan_create_without_gpu_fails_cleanly(L):
+    with pytest.raises(rg.MoEError) as ei:
+        rg.moe_plan_create(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
+    assert ei.value.code in (rg.MOE_ERR_CUDA, rg.MOE_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_null_arguments(L):
+    assert L.moe_plan_create(None, None) == rg.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_bytes(None, 10) == 0
+    assert L.moe_fwd(None, 1, None, None, None, None, 0, None) == rg.MOE_ERR_INVALID_ARG
+    st = ctypes.c_int()
+    assert L.moe_get_status(None, None, ctypes.byref(st), None) == rg.MOE_ERR_INVALID_ARG
+    assert L.moe_plan_destroy(None) == 0
+    assert L.moe_mxfp8_scale_bytes(128, 64) == 256
