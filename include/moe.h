@@ -46,7 +46,8 @@ typedef enum moe_error {
   MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* shape outside the limits listed at moe_config */
   MOE_ERR_WORKSPACE_TOO_SMALL = -3,
   MOE_ERR_CUDA = -4,               /* a CUDA runtime call failed (launch, copy, attribute) */
-  MOE_ERR_UNSUPPORTED_DEVICE = -5  /* the current device is not sm_103 */
+  MOE_ERR_UNSUPPORTED_DEVICE = -5, /* the current device is not sm_103 */
+  MOE_ERR_STATIC_SCRATCH_TOO_SMALL = -6 /* moe_route_static: request exceeds its fixed scratch */
 } moe_error;
 
 typedef enum moe_device_status {
@@ -211,6 +212,37 @@ int moe_get_status(const moe_plan* plan, const void* workspace, int* device_stat
  * thread runs moe_fwd with the same plan.
  */
 int moe_plan_set_timing_events(moe_plan* plan, void* const* events);
+
+/*
+ * Routing stage without any device allocation -- no counterpart in the paper.
+ *
+ * For callers that cannot call cudaMalloc themselves and cannot hand over a
+ * workspace: code embedded in a framework whose allocator owns all device
+ * memory, or latency-critical loops where an allocation (which can
+ * synchronise the device) is not allowed.  It runs the same router + top-k
+ * and schedule kernels as moe_fwd, but their scratch (per-chunk expert
+ * histograms, counters, status word, schedule-builder lists) lives in one
+ * fixed array inside the library, moe_route_static_scratch_bytes() bytes
+ * (512 KiB), that every GPU which loads the library keeps until the process
+ * exits.  Limits: T <= MOE_ROUTE_STATIC_MAX_TOKENS (and <= the plan's T_max);
+ * larger requests return MOE_ERR_STATIC_SCRATCH_TOO_SMALL and launch nothing.
+ *   x [T, D] bf16, W_router [E, D] bf16, b_router [E] fp32 or NULL (device)
+ *   outputs (device, all required): topk_idx [T, k] int32, topk_w [T, k] fp32,
+ *   expert_counts [E], expert_offsets [E + 1], sched [T*k, 3], route_row [T*k]
+ *   (int32, same meaning as in moe_outputs); device_status: optional device
+ *   int32 that receives the call's moe_device_status.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, which keeps the previous call's
+ * contents (the kernels clear what must start at zero): calls that overlap on
+ * the GPU -- on two streams, or from two threads -- race with each other.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_STATIC_SCRATCH_TOO_SMALL, MOE_ERR_CUDA.
+ */
+#define MOE_ROUTE_STATIC_MAX_TOKENS 16384
+int moe_route_static(const moe_plan* plan, int64_t T, const void* x, const void* W_router, const float* b_router,
+                     int32_t* topk_idx, float* topk_w, int32_t* expert_counts, int32_t* expert_offsets,
+                     int32_t* sched, int32_t* route_row, int32_t* device_status, moe_stream_t stream);
+size_t moe_route_static_scratch_bytes(void);
 
 /* Static description of an error code. */
 const char* moe_error_string(int code);

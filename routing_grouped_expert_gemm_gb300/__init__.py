@@ -25,6 +25,8 @@ MOE_ERR_UNSUPPORTED_SHAPE = -2
 MOE_ERR_WORKSPACE_TOO_SMALL = -3
 MOE_ERR_CUDA = -4
 MOE_ERR_UNSUPPORTED_DEVICE = -5
+MOE_ERR_STATIC_SCRATCH_TOO_SMALL = -6
+MOE_ROUTE_STATIC_MAX_TOKENS = 16384
 MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID = 0, 1, 2
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_PREC_BF16, MOE_PREC_MXFP8 = 0, 1
@@ -83,6 +85,10 @@ def lib():
     L.moe_get_status.restype = ctypes.c_int
     L.moe_plan_set_timing_events.argtypes = [vp, ctypes.POINTER(vp)]
     L.moe_plan_set_timing_events.restype = ctypes.c_int
+    L.moe_route_static.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_route_static.restype = ctypes.c_int
+    L.moe_route_static_scratch_bytes.argtypes = []
+    L.moe_route_static_scratch_bytes.restype = sz
     L.moe_error_string.argtypes = [ctypes.c_int]
     L.moe_error_string.restype = ctypes.c_char_p
     _lib = L
@@ -197,3 +203,19 @@ def moe_plan_set_timing_events(plan: Plan, events) -> None:
         rc = lib().moe_plan_set_timing_events(plan.handle, arr)
     if rc != MOE_OK:
         raise MoEError(rc, "moe_plan_set_timing_events")
+
+
+def moe_route_static(plan: Plan, T: int, x, W_router, b_router, topk_idx, topk_w, expert_counts, expert_offsets,
+                     sched, route_row, device_status=None, stream=None) -> None:
+    """Routing stage (top-k, g, counts, offsets, schedule table) that allocates
+    nothing: its scratch is a fixed array inside the library, for callers that
+    cannot call cudaMalloc.  Calls that overlap on the GPU race on that array."""
+    rc = lib().moe_route_static(plan.handle, T, _ptr(x), _ptr(W_router), _ptr(b_router), _ptr(topk_idx),
+                                _ptr(topk_w), _ptr(expert_counts), _ptr(expert_offsets), _ptr(sched),
+                                _ptr(route_row), _ptr(device_status), _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_route_static")
+
+
+def moe_route_static_scratch_bytes() -> int:
+    return int(lib().moe_route_static_scratch_bytes())

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
-SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu"]
+SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -8,6 +8,7 @@
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "plan.cuh"
 
 namespace moe {
 cudaError_t launch_router(const RouterMaps& maps, const FwdParams& p, cudaStream_t stream);
@@ -19,20 +20,6 @@ size_t mx_scale_bytes(int64_t rows, int64_t K);
 }  // namespace moe
 
 using namespace moe;
-
-typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-struct moe_plan {
-  moe_config cfg;
-  int device;
-  int num_sms;
-  int grid;  // persistent kernel CTAs = gather + gemm
-  encode_tiled_fn encode;
-  cudaEvent_t timing[4];  // optional, see moe_plan_set_timing_events
-  bool timed;
-};
 
 namespace {
 
@@ -112,6 +99,8 @@ const char* moe_error_string(int code) {
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case MOE_ERR_STATIC_SCRATCH_TOO_SMALL:
+      return "request exceeds the library's fixed routing scratch (T > MOE_ROUTE_STATIC_MAX_TOKENS)";
     default: return "unknown error";
   }
 }

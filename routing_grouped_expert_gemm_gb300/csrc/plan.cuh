@@ -1,0 +1,20 @@
+// Host-side state of a moe_plan (shared by the C-ABI translation units).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct moe_plan {
+  moe_config cfg;
+  int device;
+  int num_sms;
+  int grid;  // persistent kernel CTAs = gather + gemm
+  encode_tiled_fn encode;
+  cudaEvent_t timing[4];  // optional, see moe_plan_set_timing_events
+  bool timed;
+};
