@@ -57,7 +57,24 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: a smaller case with this many tokens (uniform routing)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: a smaller case with this many routed experts (uniform routing)")
     return ap.parse_args()
+
+
+def select_workload(args):
+    """The named workload, or (profiling only) a smaller case of the same D, I,
+    k, I_s with --tokens / --experts and uniform routing."""
+    shape = mi.CONFIGS[args.workload]
+    if not args.tokens and not args.experts:
+        return shape, mi.make_inputs(shape)
+    T = args.tokens or shape.T
+    E = args.experts or shape.E
+    small = mi.custom_shape(T, shape.D, shape.I, E, shape.k, shape.I_s, score=shape.score,
+                            config_id=shape.config_id + 1000)
+    return small, mi.make_inputs(small, calibration={"beta": None, "redraw": {}})
 
 
 def load_peaks():
@@ -147,8 +164,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    shape = mi.CONFIGS[args.workload]
-    inp = mi.make_inputs(shape)
+    shape, inp = select_workload(args)
     per_step_tokens = None
     times = []
     total_steps = args.warmup + args.steps
@@ -206,12 +222,11 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     rgbuild.build()
-    shape = mi.CONFIGS[args.workload]
+    t_gen = time.perf_counter()
+    shape, inp = select_workload(args)
+    t_gen = time.perf_counter() - t_gen
     if shape.precision != "bf16":
         raise SystemExit("only the bf16 path is benchmarked by this arm")
-    t_gen = time.perf_counter()
-    inp = mi.make_inputs(shape)
-    t_gen = time.perf_counter() - t_gen
 
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
