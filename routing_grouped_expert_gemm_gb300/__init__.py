@@ -17,6 +17,8 @@ import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300.so")
+if os.environ.get("MOE_TRACE_BUILD") == "1":  # profiling only: the MOE_TRACE variant of the same library
+    LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300_trace.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 
 MOE_OK = 0

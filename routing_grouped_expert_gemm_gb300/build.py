@@ -19,6 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
+TRACE_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_trace.so")
 SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -30,10 +31,10 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, verbose: bool, ptxas_v: bool) -> str:
-    obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose: bool, ptxas_v: bool, defines=(), obj_dir: str = OBJ) -> str:
+    obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-           "-c", os.path.join(CSRC, src), "-o", obj]
+           *[f"-D{d}" for d in defines], "-c", os.path.join(CSRC, src), "-o", obj]
     if ptxas_v:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -44,29 +45,34 @@ def _compile(src: str, verbose: bool, ptxas_v: bool) -> str:
     return obj
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(HERE, "..", "include", "moe.h")]
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(OBJ, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False) -> str:
+    """Build the library; trace=True builds the MOE_TRACE variant (per-CTA wait
+    timers in the persistent kernel) as _lib/libmoe_gb300_trace.so instead."""
+    lib_path = TRACE_LIB_PATH if trace else LIB_PATH
+    obj_dir = OBJ + ("_trace" if trace else "")
+    if not force and not _stale(lib_path):
+        return lib_path
+    os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
+    defines = ("MOE_TRACE",) if trace else ()
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, ptxas_v), SOURCES))
-    tmp = LIB_PATH + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, ptxas_v, defines, obj_dir), SOURCES))
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp, "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -29,7 +29,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Layout {
   size_t status, counters, meta, topk_idx, topk_w, chunk_counts, M, S, sched, route_row, mtiles, segs, tasks;
-  size_t ring_x, ring_h, h_s, Y, total;
+  size_t ring_x, ring_h, h_s, Y, trace, total;
   int64_t n_mb, n_mtiles_max, n_smtiles, n_tasks_max, n_counters, n_chunks, max_segs, R;
 };
 
@@ -69,6 +69,9 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.ring_h = take((size_t)ring_rows * c.I * 2);
   L.h_s = take((size_t)T * c.I_s * 2);
   L.Y = take((size_t)L.R * c.D * 4);
+#ifdef MOE_TRACE
+  L.trace = take(sizeof(unsigned long long) * TRACE_SLOTS * 1024);
+#endif
   L.total = off;
   return L;
 }
@@ -124,6 +127,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.minibatch < BM || c.minibatch > 32768 || c.minibatch % BM) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.ring_slots < c.lag + 1 || c.ring_slots > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((c.T_max * c.k + c.minibatch - 1) / c.minibatch > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;  // schedule smem
   if (c.gather_ctas < 1 || c.gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
   if (c.precision == MOE_PREC_MXFP8) return MOE_ERR_UNSUPPORTED_SHAPE;  // routed MXFP8 path: not built yet
 
@@ -255,6 +259,10 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.h_s = reinterpret_cast<bf16*>(ws + L.h_s);
   p.Y = reinterpret_cast<float*>(ws + L.Y);
   p.out = static_cast<bf16*>(o->out);
+#ifdef MOE_TRACE
+  p.trace = reinterpret_cast<unsigned long long*>(ws + L.trace);
+  cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * 1024, stream);
+#endif
 
   // tensor maps (raw pointers are baked in, so they are encoded per call)
   RouterMaps rm;

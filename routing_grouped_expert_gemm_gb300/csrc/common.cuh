@@ -35,7 +35,7 @@ enum : int { STATUS_OK = 0, STATUS_TIMEOUT = 1, STATUS_SCHEDULE_INVALID = 2 };
 // task kinds of the persistent kernel
 enum : int { TASK_R1 = 0, TASK_R2 = 1, TASK_S1 = 2, TASK_S2 = 3 };
 
-struct Task {      // 64 bytes
+struct __align__(16) Task {  // 64 bytes
   int kind;        // TASK_*
   int n;           // output column tile
   int e;           // routed expert (0 for the shared expert)
@@ -87,7 +87,26 @@ struct FwdParams {
   bf16* h_s;          // [T, I_s]
   float* Y;           // [R, D] fp32, token order (row j = t*k + slot)
   bf16* out;          // [T, D]
+  unsigned long long* trace;  // [grid, TRACE_SLOTS] when built with MOE_TRACE, else null
 };
+
+// Optional per-CTA timing of the persistent kernel (build with -DMOE_TRACE):
+// SM cycles spent in each kind of wait, plus start/end %globaltimer stamps.
+enum : int {
+  TR_START_NS = 0, TR_END_NS, TR_PROD_DEP, TR_PROD_EMPTY, TR_MMA_FULL, TR_MMA_TEMPTY, TR_EPI_TFULL, TR_EPI_BUSY,
+  TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_MMA_BUSY, TRACE_SLOTS = 16
+};
+#ifdef MOE_TRACE
+#define TRACE_T0() const long long _tr0 = clock64()
+#define TRACE_ADD(p, slot) \
+  do { if ((p).trace) atomicAdd((p).trace + (size_t)blockIdx.x * TRACE_SLOTS + (slot), (unsigned long long)(clock64() - _tr0)); } while (0)
+#define TRACE_SET(p, slot, v) \
+  do { if ((p).trace) (p).trace[(size_t)blockIdx.x * TRACE_SLOTS + (slot)] = (unsigned long long)(v); } while (0)
+#else
+#define TRACE_T0() do {} while (0)
+#define TRACE_ADD(p, slot) do {} while (0)
+#define TRACE_SET(p, slot, v) do {} while (0)
+#endif
 
 // counter indices
 __host__ __device__ inline int ctr_ydone() { return 0; }

@@ -46,12 +46,15 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int nv = p.D / 8;  // 16-byte vectors per row
-  constexpr int UNR = 8;
+  // a whole row in flight per warp (D <= 8192 in one pass), loads before stores
+  constexpr int UNR = 32;
   for (int m = 0; m < p.n_mb; ++m) {
     if (m >= p.slots) {
       if (threadIdx.x == 0) {
         const int need = p.meta[META_MB + 2 * (m - p.slots)];
+        TRACE_T0();
         *s_flag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), need, p.status, p.timeout_ns) ? 1 : 0;
+        TRACE_ADD(p, TR_GATHER_WAIT);
       }
       __syncthreads();
       if (*s_flag == 0) return;
@@ -60,6 +63,7 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
     const int per = (hi - lo + p.G - 1) / p.G;
     const int r0 = lo + g * per, r1 = min(hi, r0 + per);
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
+    TRACE_T0();
     for (int r = r0 + warp; r < r1; r += nwarps) {
       const int t = p.sched[(size_t)r * 3];
       const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.D);
@@ -80,7 +84,10 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
     }
     fence_proxy_async_global();
     __syncthreads();
-    if (threadIdx.x == 0) red_release_add_gpu(p.counters + ctr_filled(p, m), 1);
+    if (threadIdx.x == 0) {
+      TRACE_ADD(p, TR_GATHER_BUSY);
+      red_release_add_gpu(p.counters + ctr_filled(p, m), 1);
+    }
   }
 }
 
@@ -245,6 +252,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
+  if (threadIdx.x == 0) TRACE_SET(p, TR_START_NS, globaltimer_ns());
   const bool has_shared = p.N1s > 0;
 
   if (is_gather) {
@@ -288,12 +296,20 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         bool ok = true;
         for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
           const Task t = p.tasks[ti];
-          if (t.dep0 >= 0 && !wait_counter_ge(p.counters + t.dep0, t.need0, p.status, p.timeout_ns)) break;
-          if (t.dep1 >= 0 && !wait_counter_ge(p.counters + t.dep1, t.need1, p.status, p.timeout_ns)) break;
+          {
+            TRACE_T0();
+            if (t.dep0 >= 0 && !wait_counter_ge(p.counters + t.dep0, t.need0, p.status, p.timeout_ns)) break;
+            if (t.dep1 >= 0 && !wait_counter_ge(p.counters + t.dep1, t.need1, p.status, p.timeout_ns)) break;
+            TRACE_ADD(p, TR_PROD_DEP);
+          }
           fence_proxy_async_global();
           const Operands o = task_operands(maps, p, t);
           for (int kb = 0; kb < o.nk; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns)) { ok = false; break; }
+            {
+              TRACE_T0();
+              if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns)) { ok = false; break; }
+              TRACE_ADD(p, TR_PROD_EMPTY);
+            }
             uint8_t* sa = smem + stage * STAGE_BYTES;
             uint8_t* sb = sa + A_STAGE_BYTES;
             mbar_arrive_expect_tx(&full[stage], (uint32_t)STAGE_BYTES);
@@ -321,11 +337,19 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         bool ok = true;
         for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
           const int nk = task_nk(p, p.tasks[ti].kind);
-          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.status, p.timeout_ns)) break;
+          {
+            TRACE_T0();
+            if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.status, p.timeout_ns)) break;
+            TRACE_ADD(p, TR_MMA_TEMPTY);
+          }
           tc_fence_after();
           const uint32_t d = tmem + acc * ACC_COLS;
           for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&full[stage], phase, p.status, p.timeout_ns)) { ok = false; break; }
+            {
+              TRACE_T0();
+              if (!mbar_wait(&full[stage], phase, p.status, p.timeout_ns)) { ok = false; break; }
+              TRACE_ADD(p, TR_MMA_FULL);
+            }
             tc_fence_after();
             const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
@@ -355,14 +379,17 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         // one thread waits and decides for all four warps, so that they agree
         // on stopping and never strand each other at the named barrier
         if (threadIdx.x == 64) {
+          TRACE_T0();
           int ok = mbar_wait(&tfull[acc], acc_phase, p.status, p.timeout_ns) ? 1 : 0;
           if (ok && t.kind == TASK_S2 && !routed_done)  // the combine reads every routed output row
             ok = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
           routed_done = routed_done || (ok && t.kind == TASK_S2);
           *s_ok = ok;
+          TRACE_ADD(p, TR_EPI_TFULL);
         }
         named_bar_sync(1, 128);
         if (*s_ok == 0) break;
+        TRACE_T0();
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
         const bool valid = row < t.rows;
@@ -381,6 +408,8 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         fence_proxy_async_global();
         named_bar_sync(1, 128);
         if (threadIdx.x == 64) {
+          TRACE_ADD(p, TR_EPI_BUSY);
+          TRACE_SET(p, TR_TASKS, ti);
           if (t.done0 >= 0) red_release_add_gpu(p.counters + t.done0, 1);
           if (t.done1 >= 0) red_release_add_gpu(p.counters + t.done1, 1);
         }
@@ -397,11 +426,16 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
 
   // ---------------- combine without a shared expert: every CTA, once all routed rows are stored
   if (!has_shared) {
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+      TRACE_T0();
       *s_flag = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
+      TRACE_ADD(p, TR_FINAL_WAIT);
+    }
     __syncthreads();
     if (*s_flag) combine_role(p);
   }
+  __syncthreads();
+  if (threadIdx.x == 0) TRACE_SET(p, TR_END_NS, globaltimer_ns());
 }
 
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream) {

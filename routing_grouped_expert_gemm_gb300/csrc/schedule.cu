@@ -20,7 +20,7 @@
 
 namespace moe {
 
-__device__ void build_tasks(const FwdParams& p, const int* sS);
+__device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm);
 
 __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdParams p) {
   __shared__ int sM[E_MAX];
@@ -29,15 +29,17 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
   __shared__ uint32_t sMask[4][E_MAX];
   __shared__ int sWarp[SCHED_THREADS / 32];
 
+  extern __shared__ int dyn_smem[];
   const int c = blockIdx.x, E = p.E, k = p.k, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
 
   for (int e = tid; e < E; e += blockDim.x) {
     int tot = 0, pre = 0;
-    for (int cc = 0; cc < p.n_chunks; ++cc) {
+#pragma unroll 8
+    for (int cc = 0; cc < p.n_chunks; ++cc) {  // independent loads: unrolled so they overlap
       const int v = p.chunk_counts[(size_t)cc * E + e];
       tot += v;
-      if (cc < c) pre += v;
+      pre += cc < c ? v : 0;
     }
     sM[e] = tot;
     sPre[e] = pre;
@@ -109,163 +111,251 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
     for (int e = tid; e < E; e += blockDim.x) p.M[e] = sM[e];
     for (int e = tid; e <= E; e += blockDim.x) p.S[e] = sS[e];
     if (tid == 0 && sS[E] != p.R) raise_status(p.status, STATUS_SCHEDULE_INVALID);
-    build_tasks(p, sS);
   }
+  build_tasks(p, sS, dyn_smem);  // every CTA: CTA 0 writes the layout, all CTAs share the task fill
 }
 
 // ------------------------------------------------------------------ task list
-// Work items, in execution order:
+// Order of execution:
 //   S1 (shared expert up/gate, all tokens) ;
 //   for step s = 0 .. n_mb - 1 + lag:  R1(s) if s < n_mb ;  R2(s - lag) if s >= lag ;
 //   S2 (shared expert down projection + combine, all tokens)
-// R1(m) / R2(m): for each expert segment of minibatch m: for each column tile
-// n: for each M-tile of the segment (M-tiles of one weight slice run side by
-// side, so the slice is read from HBM once).
+// R1(m) / R2(m): for each segment of minibatch m (an expert's rows inside m),
+// for each column tile n, for each M-tile of the segment -- the M-tiles that
+// share a weight slice run side by side (slice read from HBM once) and a
+// segment's A rows stay in L2 across its column tiles.
 // A GEMM CTA takes tasks g, g + n_gemm, g + 2 n_gemm, ...; every dependency of
 // a task points to an earlier task (or to the gather, whose own dependencies
 // are earlier tasks), so the smallest unfinished task can always proceed.
 //
-// Workspace scratch (p.segs): [segments x 4] {e, mt_begin, mt_count, m},
-// then [items x 4] {kind, seg (-1 = shared), task_begin, count},
-// then [n_mb + 1] first segment of each minibatch.
-__device__ void build_tasks(const FwdParams& p, const int* sS) {
-  __shared__ int s_nitems;
-  const int max_segs = p.n_mb + p.E;
-  int* segs = p.segs;
-  int* items = p.segs + 4 * max_segs;
-  int* mb_seg = items + 4 * (2 * max_segs + 2);
-  const int tid = threadIdx.x;
+// Segments sorted by first row are in expert-major order and every
+// minibatch's segments are contiguous, so the whole layout comes from
+// per-expert counts and block-wide scans (no serial walk).
+// p.segs holds [segments x 4] {e, mt_begin, mt_count, m}.
+// Dynamic shared memory: mb_tiles[n_mb], mt_first[n_mb], step_off[n_mb + lag + 1].
 
-  if (tid == 0) {
-    int nmt = 0, nseg = 0, e = 0;
-    for (int m = 0; m < p.n_mb; ++m) {
-      const int lo = m * p.b, hi = min(p.R, lo + p.b);
-      while (e < p.E && sS[e + 1] <= lo) ++e;
-      mb_seg[m] = nseg;
-      const int mt0 = nmt;
-      for (int ee = e; ee < p.E && sS[ee] < hi; ++ee) {
-        const int s0 = max(sS[ee], lo), s1 = min(sS[ee + 1], hi);
-        if (s1 <= s0) continue;
-        const int beg = nmt;
-        if (nseg >= max_segs || nmt + (s1 - s0 + BM - 1) / BM > p.n_mtiles_max) {
-          raise_status(p.status, STATUS_SCHEDULE_INVALID);
-          break;
-        }
-        for (int r0 = s0; r0 < s1; r0 += BM) {
-          int* mt = p.mtiles + 4 * nmt;
-          mt[0] = ee;
-          mt[1] = r0;
-          mt[2] = min(BM, s1 - r0);
-          mt[3] = m;
-          ++nmt;
-        }
-        int* sg = segs + 4 * nseg;
-        sg[0] = ee;
-        sg[1] = beg;
-        sg[2] = nmt - beg;
-        sg[3] = m;
-        ++nseg;
+// exclusive scan of v[0..n) in place (shared memory), returns the total; all threads call it
+__device__ int block_exclusive_scan(int* v, int n, int* warp_tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  int carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const int x = i < n ? v[i] : 0;
+    int inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nwarps ? warp_tmp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
       }
-      p.meta[META_MB + 2 * m] = (nmt - mt0) * p.N1;
-      p.meta[META_MB + 2 * m + 1] = (nmt - mt0) * p.N2;
+      if (lane < nwarps) warp_tmp[lane] = w;
     }
-    mb_seg[p.n_mb] = nseg;
+    __syncthreads();
+    const int before = warp > 0 ? warp_tmp[warp - 1] : 0;
+    const int total = warp_tmp[nwarps - 1];
+    if (i < n) v[i] = carry + before + inc - x;
+    carry += total;
+    __syncthreads();
+  }
+  return carry;
+}
 
-    int nit = 0, ntask = 0, total_y = 0;
-    auto add = [&](int kind, int seg, int count) {
-      int* it = items + 4 * nit;
-      it[0] = kind;
-      it[1] = seg;
-      it[2] = ntask;
-      it[3] = count;
-      ++nit;
-      ntask += count;
-      if (kind == TASK_R2) total_y += count;
-    };
-    const bool shared = p.N1s > 0;
-    if (shared) add(TASK_S1, -1, p.N1s * p.n_smtiles);
-    for (int s = 0; s < p.n_mb + p.lag; ++s) {
-      if (s < p.n_mb)
-        for (int g = mb_seg[s]; g < mb_seg[s + 1]; ++g) add(TASK_R1, g, segs[4 * g + 2] * p.N1);
-      const int m = s - p.lag;
-      if (m >= 0)
-        for (int g = mb_seg[m]; g < mb_seg[m + 1]; ++g) add(TASK_R2, g, segs[4 * g + 2] * p.N2);
+// a task record as four 16-byte stores
+__device__ __forceinline__ void store_task(Task* dst, const Task& t) {
+  const int4* src = reinterpret_cast<const int4*>(&t);
+  int4* d = reinterpret_cast<int4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = src[i];
+}
+
+__device__ __forceinline__ void piece_rows(const int* sS, int e, int m, int b, int& a, int& z) {
+  a = max(sS[e], m * b);
+  z = min(sS[e + 1], (m + 1) * b);
+}
+
+__device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
+  __shared__ int s_seg[E_MAX];  // per expert: segment count, then first segment
+  __shared__ int s_mt[E_MAX];   // per expert: M-tile count, then first M-tile
+  __shared__ int s_tmp[SCHED_THREADS / 32];
+  __shared__ int s_tot[4];
+  const int E = p.E, b = p.b, n_mb = p.n_mb, tid = threadIdx.x;
+  int* mb_tiles = dsm;
+  int* mt_first = dsm + n_mb;
+  int* step_off = dsm + 2 * n_mb;
+  const int n_steps = n_mb + p.lag;
+
+  for (int m = tid; m < n_mb; m += blockDim.x) mb_tiles[m] = 0;
+  if (tid < E) {
+    int nseg = 0, ntile = 0;
+    if (sS[tid + 1] > sS[tid]) {
+      const int m0 = sS[tid] / b, m1 = (sS[tid + 1] - 1) / b;
+      nseg = m1 - m0 + 1;
+      for (int m = m0; m <= m1; ++m) {
+        int a, z;
+        piece_rows(sS, tid, m, b, a, z);
+        ntile += (z - a + BM - 1) / BM;
+      }
     }
-    // the shared expert's down projection carries the combine in its epilogue,
-    // so it comes last: its epilogue needs every routed output row
-    if (shared) add(TASK_S2, -1, p.N2s * p.n_smtiles);
-    if (ntask > p.n_tasks_max) {  // cannot happen for consistent counts; run nothing
-      raise_status(p.status, STATUS_SCHEDULE_INVALID);
-      nit = 0;
-      ntask = 0;
-      total_y = 0;
+    s_seg[tid] = nseg;
+    s_mt[tid] = ntile;
+  }
+  __syncthreads();
+  const int nseg_tot = block_exclusive_scan(s_seg, E, s_tmp);
+  const int nmt_tot = block_exclusive_scan(s_mt, E, s_tmp);
+  const bool fits = nseg_tot <= p.n_mb + E && nmt_tot <= p.n_mtiles_max;
+  if (tid == 0 && !fits) raise_status(p.status, STATUS_SCHEDULE_INVALID);
+
+  if (blockIdx.x == 0 && fits && tid < E && sS[tid + 1] > sS[tid]) {
+    const int m0 = sS[tid] / b, m1 = (sS[tid + 1] - 1) / b;
+    int g = s_seg[tid], mt = s_mt[tid];
+    for (int m = m0; m <= m1; ++m, ++g) {
+      int a, z;
+      piece_rows(sS, tid, m, b, a, z);
+      const int cnt = (z - a + BM - 1) / BM;
+      int* sg = p.segs + 4 * g;
+      sg[0] = tid;
+      sg[1] = mt;
+      sg[2] = cnt;
+      sg[3] = m;
+      mt += cnt;
     }
-    p.meta[META_N_TASKS] = ntask;
-    p.meta[META_N_MTILES] = nmt;
-    p.meta[META_TOTAL_Y] = total_y;
-    s_nitems = nit;
+  }
+  if (fits && tid < E && sS[tid + 1] > sS[tid]) {
+    const int m0 = sS[tid] / b, m1 = (sS[tid + 1] - 1) / b;
+    int mt = s_mt[tid];
+    for (int m = m0; m <= m1; ++m) {
+      int a, z;
+      piece_rows(sS, tid, m, b, a, z);
+      const int cnt = (z - a + BM - 1) / BM;
+      if (a == m * b) mt_first[m] = mt;  // exactly one segment opens each minibatch
+      atomicAdd(&mb_tiles[m], cnt);
+      mt += cnt;
+    }
   }
   __syncthreads();
 
-  const int nit = s_nitems;
-  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  for (int i = warp; i < nit; i += nwarps) {
-    const int kind = items[4 * i], seg = items[4 * i + 1], base = items[4 * i + 2], count = items[4 * i + 3];
-    for (int q = lane; q < count; q += 32) {
-      Task tk;
-      tk.kind = kind;
-      tk.dep0 = tk.dep1 = tk.done0 = tk.done1 = -1;
-      tk.need0 = tk.need1 = 0;
-      tk.pad[0] = tk.pad[1] = tk.pad[2] = 0;
-      if (seg < 0) {  // shared expert: tiles of 128 tokens
-        const int mt = q % p.n_smtiles;
-        tk.n = q / p.n_smtiles;
-        tk.e = 0;
-        tk.a_row = mt * BM;
-        tk.rows = min(BM, p.T - mt * BM);
-        tk.p0 = mt * BM;
-        tk.out_row = mt * BM;
-        if (kind == TASK_S1) {
-          tk.done0 = ctr_shready(p, mt);
-        } else {
-          tk.dep0 = ctr_shready(p, mt);
-          tk.need0 = p.N1s;
-        }
-      } else {
-        const int* sg = segs + 4 * seg;
-        const int cnt = sg[2];
-        const int mt = sg[1] + q % cnt;
-        tk.n = q / cnt;
-        const int* mtr = p.mtiles + 4 * mt;
-        const int m = mtr[3];
-        tk.e = mtr[0];
-        tk.p0 = mtr[1];
-        tk.rows = mtr[2];
-        tk.a_row = (m % p.slots) * p.b + (mtr[1] - m * p.b);
+  // per-minibatch task counts and the first task of every step
+  if (blockIdx.x == 0) {
+    for (int m = tid; m < n_mb; m += blockDim.x) {
+      p.meta[META_MB + 2 * m] = fits ? mb_tiles[m] * p.N1 : 0;
+      p.meta[META_MB + 2 * m + 1] = fits ? mb_tiles[m] * p.N2 : 0;
+    }
+  }
+  for (int s = tid; s < n_steps; s += blockDim.x) {
+    const int r1 = s < n_mb ? mb_tiles[s] * p.N1 : 0;
+    const int r2 = s - p.lag >= 0 ? mb_tiles[s - p.lag] * p.N2 : 0;
+    step_off[s] = r1 + r2;
+  }
+  __syncthreads();
+  const int n_s1 = p.N1s * p.n_smtiles, n_s2 = p.N2s * p.n_smtiles;
+  const int routed = block_exclusive_scan(step_off, n_steps, s_tmp);
+  const long long total = (long long)n_s1 + routed + n_s2;
+  if (tid == 0) {
+    const bool ok = fits && total <= p.n_tasks_max;
+    if (blockIdx.x == 0) {
+      if (!ok) raise_status(p.status, STATUS_SCHEDULE_INVALID);
+      p.meta[META_N_TASKS] = ok ? (int)total : 0;
+      p.meta[META_N_MTILES] = nmt_tot;
+      int y = 0;
+      for (int m = 0; m < n_mb; ++m) y += mb_tiles[m] * p.N2;
+      p.meta[META_TOTAL_Y] = ok ? y : 0;
+    }
+    s_tot[0] = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_tot[0]) return;
+
+  // shared-expert tasks: tiles of 128 tokens, column tile major
+  for (int q = blockIdx.x * blockDim.x + tid; q < n_s1 + n_s2; q += gridDim.x * blockDim.x) {
+    const bool down = q >= n_s1;
+    const int qq = down ? q - n_s1 : q;
+    const int mt = qq % p.n_smtiles;
+    Task tk;
+    tk.kind = down ? TASK_S2 : TASK_S1;
+    tk.n = qq / p.n_smtiles;
+    tk.e = 0;
+    tk.a_row = mt * BM;
+    tk.rows = min(BM, p.T - mt * BM);
+    tk.p0 = mt * BM;
+    tk.out_row = mt * BM;
+    tk.dep0 = down ? ctr_shready(p, mt) : -1;
+    tk.need0 = down ? p.N1s : 0;
+    tk.dep1 = -1;
+    tk.need1 = 0;
+    tk.done0 = down ? -1 : ctr_shready(p, mt);
+    tk.done1 = -1;
+    tk.pad[0] = tk.pad[1] = tk.pad[2] = 0;
+    store_task(p.tasks + (down ? (int)total - n_s2 + qq : qq), tk);
+  }
+  // routed tasks: CTA c fills experts c, c + gridDim.x, ...; its threads stride
+  // over the expert's tasks, segment by segment
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    if (sS[e + 1] <= sS[e]) continue;
+    const int m0 = sS[e] / b, m1 = (sS[e + 1] - 1) / b;
+    int mtb = s_mt[e];
+    for (int m = m0; m <= m1; ++m) {
+      int a, z;
+      piece_rows(sS, e, m, b, a, z);
+      const int cnt = (z - a + BM - 1) / BM;
+      const int slot_row = (m % p.slots) * b;
+      const int r1_base = n_s1 + step_off[m] + p.N1 * (mtb - mt_first[m]);
+      const int sr2 = m + p.lag;
+      const int r2_base =
+          n_s1 + step_off[sr2] + (sr2 < n_mb ? mb_tiles[sr2] * p.N1 : 0) + p.N2 * (mtb - mt_first[m]);
+      const int need_h = m >= p.slots ? mb_tiles[m - p.slots] * p.N2 : 0;
+      for (int q = tid; q < cnt * (p.N1 + p.N2); q += blockDim.x) {
+        const bool down = q >= cnt * p.N1;
+        const int qq = down ? q - cnt * p.N1 : q;
+        const int i = qq % cnt;
+        const int r0 = a + i * BM;
+        Task tk;
+        tk.kind = down ? TASK_R2 : TASK_R1;
+        tk.n = qq / cnt;
+        tk.e = e;
+        tk.a_row = slot_row + (r0 - m * b);
+        tk.rows = min(BM, z - r0);
+        tk.p0 = r0;
         tk.out_row = tk.a_row;
-        if (kind == TASK_R1) {
+        if (!down) {
           tk.dep0 = ctr_filled(p, m);
           tk.need0 = p.G;
-          if (m >= p.slots) {
-            tk.dep1 = ctr_r2(p, m - p.slots);
-            tk.need1 = p.meta[META_MB + 2 * (m - p.slots) + 1];
-          }
-          tk.done0 = ctr_hready(p, mt);
+          tk.dep1 = m >= p.slots ? ctr_r2(p, m - p.slots) : -1;
+          tk.need1 = need_h;
+          tk.done0 = ctr_hready(p, mtb + i);
           tk.done1 = ctr_r1(p, m);
         } else {
-          tk.dep0 = ctr_hready(p, mt);
+          tk.dep0 = ctr_hready(p, mtb + i);
           tk.need0 = p.N1;
+          tk.dep1 = -1;
+          tk.need1 = 0;
           tk.done0 = ctr_r2(p, m);
           tk.done1 = ctr_ydone();
         }
+        tk.pad[0] = tk.pad[1] = tk.pad[2] = 0;
+        store_task(p.tasks + (down ? r2_base : r1_base) + qq, tk);
       }
-      p.tasks[base + q] = tk;
+      mtb += cnt;
     }
   }
 }
 
+int schedule_smem_bytes(const FwdParams& p) { return (int)sizeof(int) * (3 * p.n_mb + p.lag + 1); }
+
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
-  schedule_kernel<<<p.n_chunks, SCHED_THREADS, 0, stream>>>(p);
+  const int smem = schedule_smem_bytes(p);
+  if (smem > 48 * 1024) {
+    const cudaError_t err = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+  }
+  schedule_kernel<<<p.n_chunks, SCHED_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
