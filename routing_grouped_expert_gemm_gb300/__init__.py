@@ -91,6 +91,8 @@ def lib():
     L.moe_route_static.restype = ctypes.c_int
     L.moe_route_static_scratch_bytes.argtypes = []
     L.moe_route_static_scratch_bytes.restype = sz
+    L.moe_testing_mx_tile.argtypes = [vp, vp, vp, vp, vp]
+    L.moe_testing_mx_tile.restype = ctypes.c_int
     L.moe_error_string.argtypes = [ctypes.c_int]
     L.moe_error_string.restype = ctypes.c_char_p
     _lib = L
@@ -98,9 +100,9 @@ def lib():
 
 
 def declared_functions() -> list[str]:
-    """Function names declared in include/moe.h."""
-    with open(HEADER_PATH) as f:
-        text = f.read()
+    """Function names declared in include/*.h (the ABI and the test hooks)."""
+    inc = os.path.dirname(HEADER_PATH)
+    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)))
 
 

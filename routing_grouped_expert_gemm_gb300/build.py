@@ -20,7 +20,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
 TRACE_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_trace.so")
-SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu"]
+SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu", "probe_mx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,7 +49,8 @@ def _stale(lib_path: str) -> bool:
     if not os.path.exists(lib_path):
         return True
     t = os.path.getmtime(lib_path)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(HERE, "..", "include", "moe.h")]
+    inc = os.path.join(HERE, "..", "include")
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(inc, f) for f in os.listdir(inc)]
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 

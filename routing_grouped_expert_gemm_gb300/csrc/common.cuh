@@ -94,7 +94,8 @@ struct FwdParams {
 // SM cycles spent in each kind of wait, plus start/end %globaltimer stamps.
 enum : int {
   TR_START_NS = 0, TR_END_NS, TR_PROD_DEP, TR_PROD_EMPTY, TR_MMA_FULL, TR_MMA_TEMPTY, TR_EPI_TFULL, TR_EPI_BUSY,
-  TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_MMA_BUSY, TRACE_SLOTS = 16
+  TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_EPI_R1, TR_EPI_R2, TR_EPI_S1, TR_EPI_S2,
+  TRACE_SLOTS = 16
 };
 #ifdef MOE_TRACE
 #define TRACE_T0() const long long _tr0 = clock64()

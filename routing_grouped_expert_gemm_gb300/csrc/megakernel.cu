@@ -38,7 +38,8 @@ __device__ __forceinline__ uint8_t* align_1024_mk(uint8_t* p) {
 }
 
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
-constexpr int MEGA_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
+constexpr int MEGA_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
 
 // ------------------------------------------------------------------ gather (dispatch)
 // Ring slot m % slots receives schedule rows [m b, min((m+1) b, R)) of x.
@@ -142,33 +143,83 @@ __device__ __forceinline__ void store_row_bf16x32(bf16* dst, const float* v) {
   }
 }
 
-__device__ void epilogue_swiglu(uint32_t taddr, bf16* dst_row, bool valid) {
-  // columns [0,128) = up, [128,256) = gate; h = SiLU(gate) * up
+// Epilogue data movement: each warp owns 32 tile rows (TMEM lanes).  A
+// tcgen05.ld gives lane r the 32 columns of row r; the warp stages that 32x32
+// block in shared memory (row stride 33 floats: conflict-free both ways) and
+// re-reads it so that lane l handles row 4i + l/8, columns 4 (l%8) .. +3:
+// every warp store then covers 4 rows x a contiguous 32-column segment.
+struct EpiStage {
+  float v[32][33];
+  float g[32][TOPK_MAX];  // router weights of the warp's 32 tokens (combine)
+};
+static_assert(sizeof(EpiStage) == 6272, "epilogue staging size");
+
+__device__ __forceinline__ void stage_block(EpiStage& st, const float* v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) st.v[lane][j] = v[j];
+  __syncwarp();
+}
+
+__device__ __forceinline__ float4 staged4(const EpiStage& st, int rr, int cc) {
+  return make_float4(st.v[rr][cc], st.v[rr][cc + 1], st.v[rr][cc + 2], st.v[rr][cc + 3]);
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(float4 f) {
+  return make_uint2(pack_bf16x2(f.x, f.y), pack_bf16x2(f.z, f.w));
+}
+
+// up/gate tile -> h = SiLU(gate) * up (bf16): TMEM columns [0,128) up, [128,256) gate.
+// dst: row 0 of the warp's rows, column 0 of the tile; ld: row stride (elements).
+__device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t ld, int nrows, uint64_t* tempty) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < BN_UP; c += 32) {
     uint32_t u[32], g[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, u);
     tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + c), g);
     tmem_ld_wait();
+    if (c + 32 == BN_UP) {  // last TMEM read of this tile: hand the accumulator back
+      tc_fence_before();
+      mbar_arrive(tempty);
+    }
     float h[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) h[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-    if (valid) store_row_bf16x32(dst_row + c, h);
+    stage_block(st, h);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
+      if (rr < nrows) *reinterpret_cast<uint2*>(dst + (size_t)rr * ld + c + cc) = pack_bf16x4(staged4(st, rr, cc));
+    }
+    __syncwarp();
   }
 }
 
-// routed expert output row -> fp32 staging row (the weighted sum reads it back)
-__device__ void epilogue_copy_f32(uint32_t taddr, float* dst_row, bool valid) {
+// routed down-projection tile -> fp32 staging rows Y[j] (j from the schedule table)
+__device__ void epilogue_copy_f32(uint32_t taddr, EpiStage& st, float* Y, size_t D, int col0, int j_mine, int nrows,
+                                  uint64_t* tempty) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < BN_DOWN; c += 32) {
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
-    if (valid) {
-      uint4* d = reinterpret_cast<uint4*>(dst_row + c);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) d[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    if (c + 32 == BN_DOWN) {
+      tc_fence_before();
+      mbar_arrive(tempty);
     }
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    stage_block(st, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
+      const int jr = __shfl_sync(0xffffffffu, j_mine, rr);
+      if (rr < nrows) *reinterpret_cast<float4*>(Y + (size_t)jr * D + col0 + c + cc) = staged4(st, rr, cc);
+    }
+    __syncwarp();
   }
 }
 
@@ -200,22 +251,59 @@ __device__ __forceinline__ void load_g(const FwdParams& p, int t, bool valid, fl
   for (int s = 0; s < TOPK_MAX; ++s) g[s] = (valid && s < p.k) ? p.topk_w[(size_t)t * p.k + s] : 0.0f;
 }
 
-// shared-expert down projection + combine: thread = token row of the tile
-__device__ void epilogue_shared_combine(uint32_t taddr, const FwdParams& p, int t, int col0, bool valid) {
-  float g[TOPK_MAX];
-  load_g(p, t, valid, g);
+// shared-expert down projection + combine: out = bf16(y_s + sum_slot g * Y[t k + slot]),
+// y_s in fp32 straight from TMEM; t0 = token of the warp's first row
+__device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdParams& p, int t0, int col0,
+                                        int nrows, uint64_t* tempty) {
+  const int lane = threadIdx.x & 31;
+  const int k = p.k;
+#pragma unroll
+  for (int s = 0; s < TOPK_MAX; ++s) st.g[lane][s] = (lane < nrows && s < k) ? p.topk_w[(size_t)(t0 + lane) * k + s] : 0.0f;
+  // the k staging rows of a token are read once: ask L2 for them two chunks
+  // ahead (lane = row; one 128-byte line per slot and chunk)
+  const float* yrow = p.Y + (size_t)(t0 + lane) * k * p.D + col0;
+  auto prefetch_chunk = [&](int c) {
+    if (lane < nrows && c < BN_DOWN)
+      for (int s = 0; s < k; ++s) prefetch_l2(yrow + (size_t)s * p.D + c);
+  };
+  prefetch_chunk(0);
+  prefetch_chunk(32);
 #pragma unroll 1
   for (int c = 0; c < BN_DOWN; c += 32) {
+    prefetch_chunk(c + 64);
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
-    float acc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
-    if (valid) {
-      accumulate_routed(p, t, col0 + c, g, acc);
-      store_row_bf16x32(p.out + (size_t)t * p.D + col0 + c, acc);
+    if (c + 32 == BN_DOWN) {
+      tc_fence_before();
+      mbar_arrive(tempty);
     }
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    stage_block(st, v);
+#pragma unroll 2
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
+      if (rr < nrows) {
+        const int t = t0 + rr;
+        float4 acc = staged4(st, rr, cc);
+        const float* y = p.Y + (size_t)t * k * p.D + col0 + c + cc;
+#pragma unroll
+        for (int s = 0; s < TOPK_MAX; ++s) {
+          if (s < k) {
+            const float gs = st.g[rr][s];
+            const float4 f = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s * p.D));
+            acc.x = fmaf(gs, f.x, acc.x);
+            acc.y = fmaf(gs, f.y, acc.y);
+            acc.z = fmaf(gs, f.z, acc.z);
+            acc.w = fmaf(gs, f.w, acc.w);
+          }
+        }
+        *reinterpret_cast<uint2*>(p.out + (size_t)t * p.D + col0 + c + cc) = pack_bf16x4(acc);
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -249,6 +337,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = s_flag + 1;
+  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + STAGES * STAGE_BYTES + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
@@ -392,23 +481,26 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         TRACE_T0();
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
-        const bool valid = row < t.rows;
+        const int r0 = q * 32;                        // the warp's first tile row
+        const int nrows = min(32, max(0, t.rows - r0));  // its valid rows
+        EpiStage& st = epi[q];
         if (t.kind == TASK_R1) {
-          epilogue_swiglu(taddr, p.ring_h + (size_t)(t.out_row + row) * p.I + t.n * BN_UP, valid);
+          epilogue_swiglu(taddr, st, p.ring_h + (size_t)(t.out_row + r0) * p.I + t.n * BN_UP, p.I, nrows, &tempty[acc]);
         } else if (t.kind == TASK_S1) {
-          epilogue_swiglu(taddr, p.h_s + (size_t)(t.out_row + row) * p.I_s + t.n * BN_UP, valid);
+          epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows,
+                          &tempty[acc]);
         } else if (t.kind == TASK_R2) {
-          const int j = valid ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
-          epilogue_copy_f32(taddr, p.Y + (size_t)j * p.D + t.n * BN_DOWN, valid);
+          const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
+          epilogue_copy_f32(taddr, st, p.Y, p.D, t.n * BN_DOWN, j, nrows, &tempty[acc]);
         } else {
-          epilogue_shared_combine(taddr, p, t.out_row + row, t.n * BN_DOWN, valid);
+          epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, &tempty[acc]);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        fence_proxy_async_global();
+        // h tiles are read back by TMA (async proxy); Y and out only by plain loads
+        if (t.kind == TASK_R1 || t.kind == TASK_S1) fence_proxy_async_global();
         named_bar_sync(1, 128);
         if (threadIdx.x == 64) {
           TRACE_ADD(p, TR_EPI_BUSY);
+          TRACE_ADD(p, TR_EPI_R1 + t.kind);
           TRACE_SET(p, TR_TASKS, ti);
           if (t.done0 >= 0) red_release_add_gpu(p.counters + t.done0, 1);
           if (t.done1 >= 0) red_release_add_gpu(p.counters + t.done1, 1);
