@@ -160,9 +160,21 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Copy 128 lanes x 128 bits of scale factors from shared memory into TMEM.
-__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+// Copy a 32-row x 128-bit block (512 contiguous bytes of shared memory) into
+// TMEM lanes 0..31 x 4 columns, replicated into all four lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+// Descriptor of a 512-byte block of 32 rows x 16 bytes, no swizzle: core
+// matrices of 8 rows x 16 B stacked 128 B apart.
+__device__ __forceinline__ uint64_t sdesc_sf_block(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
