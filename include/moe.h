@@ -58,6 +58,7 @@ typedef enum moe_device_status {
 
 typedef enum moe_score_fn { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_fn;
 typedef enum moe_precision { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precision;
+typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe_dispatch;
 
 /*
  * Layer shape and execution knobs.
@@ -74,8 +75,14 @@ typedef enum moe_precision { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precisi
  *              128..32768 (Sec. 3.2 sweeps 512..32768)
  *   ring_slots minibatch slots in the ring (>= lag + 1); ring_slots * minibatch
  *              >= T*k gives the over-allocated (no wrap) buffer of Sec. 3.3
- *   gather_ctas  CTAs (one per SM) that only gather tokens, >= 1 (Sec. 3.4
- *              "Computation-Communication SM Tuning")
+ *   dispatch   MOE_DISPATCH_RING: gather CTAs copy the routed tokens into the
+ *              ring of minibatches (the pages' communication SMs);
+ *              MOE_DISPATCH_DIRECT: the GEMM CTAs' TMA producers fetch each
+ *              tile's token rows straight from x (tile::gather4), no gather
+ *              CTAs and no x ring (MXFP8: x is quantised once per token first)
+ *   gather_ctas  ring dispatch: CTAs (one per SM) that only gather tokens, >= 1
+ *              (Sec. 3.4 "Computation-Communication SM Tuning"); ignored for
+ *              direct dispatch
  *   gemm_ctas  CTAs that run expert GEMMs; 0 = all remaining SMs
  *   lag        0: down projections of minibatch m follow its up/gate tiles;
  *              1: they follow the up/gate tiles of minibatch m + 1
@@ -98,7 +105,8 @@ typedef struct moe_config {
   int32_t gemm_ctas;
   int32_t lag;
   int32_t timeout_ms;
-  int32_t reserved[4];
+  int32_t dispatch;
+  int32_t reserved[3];
 } moe_config;
 
 /*
@@ -170,11 +178,16 @@ size_t moe_workspace_bytes(const moe_plan* plan, int64_t T);
 
 /*
  * MXFP8 weight pre-quantisation (Sec. 3.4 "MXFP8 Support", OCP MX v1.0):
- * W [rows, K] bf16 (device), K multiple of 32 -> q [rows, K] E4M3 codes and
- * scales (E8M0, one per 32 consecutive K elements) in the library's layout,
- * moe_mxfp8_scale_bytes(rows, K) bytes.  Block scale X = 2^(floor(log2 amax)
- * - 8), elements rounded to nearest-even and saturated at +-448; an all-zero
- * block gets X = 2^-127.  Asynchronous on `stream`.
+ * W [rows, K] bf16 (device), rows and K multiples of 128 -> q [rows, K] E4M3
+ * codes and scales (E8M0, one per 32 consecutive K elements),
+ * moe_mxfp8_scale_bytes(rows, K) = rows * K / 32 bytes.  Block scale
+ * X = 2^(floor(log2 amax) - 8), elements rounded to nearest-even and saturated
+ * at +-448; an all-zero block gets X = 2^-127.  Scale layout: 512-byte blocks
+ * ordered [rows/128][K/128], each holding 128 rows x 4 blocks of 32 with the
+ * scale of (row r, block kb) at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + kb
+ * (the layout the block-scaled tensor-core MMA reads).  A stacked [E, I, D]
+ * weight is quantised as rows = E * I.  Asynchronous on `stream`.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_CUDA.
  */
 int moe_quantize_mxfp8(const moe_plan* plan, const void* W, int64_t rows, int64_t K, uint8_t* q,
                        uint8_t* scales, moe_stream_t stream);

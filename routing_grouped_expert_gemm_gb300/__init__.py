@@ -32,6 +32,7 @@ MOE_ROUTE_STATIC_MAX_TOKENS = 16384
 MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID = 0, 1, 2
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_PREC_BF16, MOE_PREC_MXFP8 = 0, 1
+MOE_DISPATCH_RING, MOE_DISPATCH_DIRECT = 0, 1
 
 
 class MoEError(RuntimeError):
@@ -45,7 +46,7 @@ class moe_config(ctypes.Structure):
                 ("k", ctypes.c_int64), ("I_s", ctypes.c_int64), ("score_fn", ctypes.c_int32),
                 ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
                 ("gather_ctas", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32), ("lag", ctypes.c_int32),
-                ("timeout_ms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("timeout_ms", ctypes.c_int32), ("dispatch", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class moe_weights(ctypes.Structure):
@@ -141,13 +142,15 @@ class Plan:
 
 
 def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
-                    ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0) -> Plan:
+                    ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0, dispatch=MOE_DISPATCH_RING) -> Plan:
     if isinstance(score_fn, str):
         score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
     if isinstance(precision, str):
         precision = {"bf16": MOE_PREC_BF16, "mxfp8": MOE_PREC_MXFP8}[precision]
+    if isinstance(dispatch, str):
+        dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
-                     lag, timeout_ms)
+                     lag, timeout_ms, dispatch)
     h = ctypes.c_void_p()
     rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
     if rc != MOE_OK:

@@ -16,6 +16,7 @@ cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream);
 int megakernel_smem_bytes();
 cudaError_t launch_mx_quantize(const bf16* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st);
 size_t mx_scale_bytes(int64_t rows, int64_t K);
 }  // namespace moe
 
@@ -29,7 +30,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Layout {
   size_t status, counters, meta, topk_idx, topk_w, chunk_counts, M, S, sched, route_row, mtiles, segs, tasks;
-  size_t ring_x, ring_h, h_s, Y, trace, total;
+  size_t ring_x, ring_h, sfx, sfh, xq, xs, h_s, Y, trace, total;
   int64_t n_mb, n_mtiles_max, n_smtiles, n_tasks_max, n_counters, n_chunks, max_segs, R;
 };
 
@@ -53,7 +54,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   };
   L.status = take(sizeof(int));
   L.counters = take(sizeof(int) * L.n_counters);
-  L.meta = take(sizeof(int) * (META_MB + 2 * L.n_mb));
+  L.meta = take(sizeof(int) * (META_MB + 4 * L.n_mb));
   L.topk_idx = take(sizeof(int) * L.R);
   L.topk_w = take(sizeof(float) * L.R);
   L.chunk_counts = take(sizeof(int) * L.n_chunks * c.E);
@@ -65,15 +66,34 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.segs = take(sizeof(int) * (4 * L.max_segs + 4 * (2 * L.max_segs + 2) + L.n_mb + 1));
   L.tasks = take(sizeof(Task) * L.n_tasks_max);
   const int64_t ring_rows = (int64_t)c.ring_slots * c.minibatch;
-  L.ring_x = take((size_t)ring_rows * c.D * 2);
-  L.ring_h = take((size_t)ring_rows * c.I * 2);
+  const bool mx = c.precision == MOE_PREC_MXFP8;
+  const bool direct = c.dispatch == MOE_DISPATCH_DIRECT;
+  const size_t elem = mx ? 1 : 2;  // E4M3 codes or bf16 in the rings
+  L.ring_x = take(direct ? 0 : (size_t)ring_rows * c.D * elem);
+  L.ring_h = take((size_t)ring_rows * c.I * elem);
+  L.sfx = take(mx && !direct ? (size_t)L.n_mtiles_max * (c.D / BK_MX) * SF_BLOCK_BYTES : 0);
+  L.xq = take(mx && direct ? (size_t)T * c.D : 0);
+  L.xs = take(mx && direct ? (size_t)T * (c.D / 32) : 0);
+  L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
-  L.Y = take((size_t)L.R * c.D * 4);
+  L.Y = take((size_t)L.R * c.D * 2);
 #ifdef MOE_TRACE
   L.trace = take(sizeof(unsigned long long) * TRACE_SLOTS * 1024);
 #endif
   L.total = off;
   return L;
+}
+
+// E4M3 codes, one byte each: 128-byte rows of the box like the bf16 maps
+int encode_u8_2d(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {BK_MX, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = pl->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
 int encode_bf16_2d(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
@@ -112,9 +132,10 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (!cfg_in || !out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   moe_config c = *cfg_in;
+  if (c.dispatch != MOE_DISPATCH_RING && c.dispatch != MOE_DISPATCH_DIRECT) return MOE_ERR_INVALID_ARG;
   if (c.minibatch == 0) c.minibatch = 8192;
   if (c.ring_slots == 0) c.ring_slots = 4;
-  if (c.gather_ctas == 0) c.gather_ctas = 8;
+  if (c.gather_ctas == 0 && c.dispatch == MOE_DISPATCH_RING) c.gather_ctas = 8;
   if (c.timeout_ms <= 0) c.timeout_ms = 2000;
   if (c.lag < 0 || c.lag > 1) return MOE_ERR_INVALID_ARG;
   if (c.score_fn != MOE_SCORE_SIGMOID && c.score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
@@ -128,8 +149,8 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.minibatch < BM || c.minibatch > 32768 || c.minibatch % BM) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.ring_slots < c.lag + 1 || c.ring_slots > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((c.T_max * c.k + c.minibatch - 1) / c.minibatch > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;  // schedule smem
-  if (c.gather_ctas < 1 || c.gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
-  if (c.precision == MOE_PREC_MXFP8) return MOE_ERR_UNSUPPORTED_SHAPE;  // routed MXFP8 path: not built yet
+  if (c.dispatch == MOE_DISPATCH_DIRECT) c.gather_ctas = 0;  // the GEMM producers gather
+  if ((c.dispatch == MOE_DISPATCH_RING && c.gather_ctas < 1) || c.gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -186,7 +207,8 @@ size_t moe_mxfp8_scale_bytes(int64_t rows, int64_t K) { return mx_scale_bytes(ro
 
 int moe_quantize_mxfp8(const moe_plan* plan, const void* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* scales,
                        moe_stream_t stream) {
-  if (!plan || !W || !q || !scales || rows < 1 || K < 32 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (!plan || !W || !q || !scales || rows < 1 || K < 128) return MOE_ERR_INVALID_ARG;
+  if (rows % 128 || K % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
   return launch_mx_quantize(static_cast<const bf16*>(W), rows, K, q, scales, (cudaStream_t)stream) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
@@ -201,6 +223,10 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
     return MOE_ERR_INVALID_ARG;
   const bool shared = w->Ws_up || w->Ws_gate || w->Ws_down;
   if (shared && (!w->Ws_up || !w->Ws_gate || !w->Ws_down || c.I_s == 0)) return MOE_ERR_INVALID_ARG;
+  const bool mx = c.precision == MOE_PREC_MXFP8;
+  if (mx && (!w->W_up_scale || !w->W_gate_scale || !w->W_down_scale)) return MOE_ERR_INVALID_ARG;
+  if (mx && (!aligned16(w->W_up_scale) || !aligned16(w->W_gate_scale) || !aligned16(w->W_down_scale)))
+    return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, w->W_router, w->W_up, w->W_gate, w->W_down, o->out, workspace};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -221,6 +247,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.k = (int)c.k;
   p.I_s = shared ? (int)c.I_s : 0;
   p.score_fn = c.score_fn;
+  p.mx = mx ? 1 : 0;
+  p.direct = c.dispatch == MOE_DISPATCH_DIRECT ? 1 : 0;
   p.b = c.minibatch;
   p.slots = c.ring_slots;
   p.G = c.gather_ctas;
@@ -256,8 +284,15 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.tasks = reinterpret_cast<Task*>(ws + L.tasks);
   p.ring_x = reinterpret_cast<bf16*>(ws + L.ring_x);
   p.ring_h = reinterpret_cast<bf16*>(ws + L.ring_h);
+  p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
+  p.xq = mx && p.direct ? ws + L.xq : nullptr;
+  p.xs = mx && p.direct ? ws + L.xs : nullptr;
+  p.sfh = mx ? ws + L.sfh : nullptr;
+  p.w_up_sf = mx ? w->W_up_scale : nullptr;
+  p.w_gate_sf = mx ? w->W_gate_scale : nullptr;
+  p.w_down_sf = mx ? w->W_down_scale : nullptr;
   p.h_s = reinterpret_cast<bf16*>(ws + L.h_s);
-  p.Y = reinterpret_cast<float*>(ws + L.Y);
+  p.Y = reinterpret_cast<__half*>(ws + L.Y);
   p.out = static_cast<bf16*>(o->out);
 #ifdef MOE_TRACE
   p.trace = reinterpret_cast<unsigned long long*>(ws + L.trace);
@@ -275,11 +310,25 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   rc |= encode_bf16_2d(pl, &rm.x, x, T, c.D, BM);
   rc |= encode_bf16_2d(pl, &rm.wr, w->W_router, c.E, c.D, wr_box);
   rc |= encode_bf16_2d(pl, &tm.x, x, T, c.D, BM);
-  rc |= encode_bf16_2d(pl, &tm.ring_x, p.ring_x, ring_rows, c.D, BM);
-  rc |= encode_bf16_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);
-  rc |= encode_bf16_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
-  rc |= encode_bf16_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
-  rc |= encode_bf16_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, BN_DOWN);
+  if (p.direct) {  // one-row boxes for tile::gather4 from x (bf16) or its E4M3 copy
+    if (mx)
+      rc |= encode_u8_2d(pl, &tm.x_rows, p.xq, T, c.D, 1);
+    else
+      rc |= encode_bf16_2d(pl, &tm.x_rows, x, T, c.D, 1);
+  }
+  if (mx) {  // routed operands as E4M3 codes
+    if (!p.direct) rc |= encode_u8_2d(pl, &tm.ring_x, p.ring_x, ring_rows, c.D, BM);
+    rc |= encode_u8_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);
+    rc |= encode_u8_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
+    rc |= encode_u8_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
+    rc |= encode_u8_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, BN_DOWN);
+  } else {
+    if (!p.direct) rc |= encode_bf16_2d(pl, &tm.ring_x, p.ring_x, ring_rows, c.D, BM);
+    rc |= encode_bf16_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);
+    rc |= encode_bf16_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
+    rc |= encode_bf16_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
+    rc |= encode_bf16_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, BN_DOWN);
+  }
   if (shared) {
     rc |= encode_bf16_2d(pl, &tm.ws_up, w->Ws_up, c.I_s, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.ws_gate, w->Ws_gate, c.I_s, c.D, BN_UP);
@@ -293,6 +342,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   if (pl->timed && cudaEventRecord(pl->timing[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_schedule(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mx && p.direct && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (launch_megakernel(tm, p, pl->grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -19,9 +21,18 @@ constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit inputs
 constexpr int BN_UP = 128;       // intermediate columns per GEMM1 tile (x2: up and gate)
 constexpr int BN_DOWN = 256;     // output columns per GEMM2 tile
 constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KB
+constexpr int A_STAGE_BYTES = BM * BK * 2;        // 16 KB (= 128 rows x 128 B, also in MXFP8)
 constexpr int B_STAGE_BYTES = 256 * BK * 2;       // 32 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+// MXFP8: a K step is 128 E4M3 codes (one 128-byte swizzle atom per row) plus
+// the E8M0 scale blocks of A (512 B) and of B's two 128-row halves (1 KB)
+constexpr int BK_MX = 128;
+constexpr int SF_BLOCK_BYTES = 512;               // 128 rows x 4 K-blocks of 32
+constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK_BYTES;
+constexpr int MX_STAGE_TX = STAGE_BYTES + SF_STAGE_BYTES;
+constexpr int STAGE_STRIDE = 51200;               // 1024-aligned stage pitch (BF16 and MXFP8)
+static_assert(STAGE_BYTES + SF_STAGE_BYTES <= STAGE_STRIDE && STAGE_STRIDE % 1024 == 0, "stage pitch");
+constexpr int SF_TMEM_COL = 256;                  // MXFP8: scale columns after the single accumulator
 constexpr int ACC_COLS = 256;    // fp32 accumulator columns per tile
 constexpr int MEGA_THREADS = 256;  // 8 warps
 constexpr int ROUTER_THREADS = 192;
@@ -46,17 +57,21 @@ struct __align__(16) Task {  // 64 bytes
   int dep0, need0; // wait until counters[dep0] >= need0 (dep < 0: none)
   int dep1, need1;
   int done0, done1;  // counters incremented when the tile is stored (-1: none)
-  int pad[3];
+  int mt;            // global M-tile index (routed) / token tile (shared)
+  int pad[2];
 };
 static_assert(sizeof(Task) == 64, "task record is 64 bytes");
 
 // meta block written by the schedule kernel (int32 offsets)
 enum : int { META_N_TASKS = 0, META_N_MTILES = 1, META_TOTAL_Y = 2 /* R2 tasks */, META_MB = 4 };
-// META_MB + 2*m: R1 task count of minibatch m; META_MB + 2*m + 1: R2 task count
+// per minibatch m, META_MB + 4 m + {0: R1 task count, 1: R2 task count,
+// 2: first M-tile, 3: M-tile count}
 
 struct FwdParams {
   int T, D, I, E, k, I_s;
   int score_fn;
+  int mx;               // routed experts in MXFP8 (1) or BF16 (0)
+  int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
   int b, slots, G, n_gemm, lag;
   int n_mb, R;          // minibatches, routes (T*k)
   int N1, N2, N1s, N2s; // column tiles: I/128, D/256, I_s/128, D/256
@@ -79,13 +94,20 @@ struct FwdParams {
   int* S;             // [E+1]
   int* sched;         // [R,3] {src_index t, expert e, dst_index j}
   int* route_row;     // [R]
-  int* mtiles;        // [n_mtiles_max, 4] {e, p0, rows, m}
+  int* mtiles;        // [n_mtiles_max, 4] {e, p0, rows, m}, row order
   int* segs;          // scratch for the task builder
   Task* tasks;        // [n_tasks_max]
-  bf16* ring_x;       // [slots*b, D]
-  bf16* ring_h;       // [slots*b, I]
+  bf16* ring_x;       // [slots*b, D] (MXFP8: E4M3 codes, 1 byte each)
+  bf16* ring_h;       // [slots*b, I] (MXFP8: E4M3 codes)
+  uint8_t* sfx;       // MXFP8 ring dispatch: scale blocks of the gathered x, [n_mtiles_max][D/128][512 B]
+  uint8_t* xq;        // MXFP8 direct dispatch: x quantised once per token, [T, D] E4M3
+  uint8_t* xs;        // ... and its E8M0 scales, [T, D/32] row-major
+  uint8_t* sfh;       // MXFP8: scale blocks of h, [n_mtiles_max][I/128][512 B]
+  const uint8_t* w_up_sf;    // MXFP8 weight scale blocks (moe_quantize_mxfp8 layout)
+  const uint8_t* w_gate_sf;
+  const uint8_t* w_down_sf;
   bf16* h_s;          // [T, I_s]
-  float* Y;           // [R, D] fp32, token order (row j = t*k + slot)
+  __half* Y;          // [R, D] fp16, token order (row j = t*k + slot)
   bf16* out;          // [T, D]
   unsigned long long* trace;  // [grid, TRACE_SLOTS] when built with MOE_TRACE, else null
 };
@@ -122,6 +144,7 @@ __host__ __device__ inline int n_counters(const FwdParams& p) { return 1 + 3 * p
 
 struct TensorMaps {
   CUtensorMap x;        // [T, D]            box {64, 128}
+  CUtensorMap x_rows;   // direct dispatch: [T, D] bf16 box {64, 1} or E4M3 box {128, 1} (tile::gather4)
   CUtensorMap ring_x;   // [slots*b, D]      box {64, 128}
   CUtensorMap w_up;     // [E*I, D]          box {64, 128}
   CUtensorMap w_gate;   // [E*I, D]          box {64, 128}
@@ -187,5 +210,46 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 
 __device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + __expf(-v)); }
+
+// OCP MX v1.0, MXFP8 E4M3 block of 32: X = 2^(floor(log2 amax) - 8), codes =
+// E4M3(v / X) rounded to nearest-even and saturated at +-448; an all-zero block
+// gets the code 0 (X = 2^-127).  Returns the E8M0 code; q receives the codes.
+__device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint32_t* q) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  if (amax == 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = 0;
+    return 0;
+  }
+  int se = ilogbf(amax) - 8;
+  se = max(-127, min(127, se));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[4 * i + j], -se), __NV_SATFINITE, __NV_E4M3) << (8 * j);
+    q[i] = w;
+  }
+  return (uint32_t)(se + 127);
+}
+
+// 32 bf16 values (64 bytes, 16-byte aligned) -> fp32
+__device__ __forceinline__ void load_bf16x32(const bf16* src, float* v) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 w = __ldg(s4 + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[8 * i + 2 * j] = f.x;
+      v[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
 
 }  // namespace moe

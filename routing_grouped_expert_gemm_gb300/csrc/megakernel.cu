@@ -19,8 +19,8 @@
 //    output never leaves TMEM in fp32 before it is added).
 //  * Sec. 3.4 "Determinism": no floating-point atomics; every output element
 //    is produced by one tile with a fixed K order, and the weighted sum runs
-//    in a fixed slot order from a token-order fp32 staging buffer (fp32 so
-//    that the sum rounds once, at the bf16 output).
+//    in a fixed slot order from a token-order fp16 staging buffer (10
+//    mantissa bits: the sum's error stays below the bf16 output rounding).
 // The expert FFN is the one of Sec. 2.1 / the blog's E_i(x) with SiLU:
 // h = SiLU(x W_gate^T) * (x W_up^T) in fp32 from TMEM, stored bf16; y = h W_down^T.
 //
@@ -29,6 +29,8 @@
 // buffers), warps 2-5 drain TMEM (tcgen05.ld), apply the epilogue and store.
 // A GEMM1 tile is 128 rows x (128 up + 128 gate) columns; a GEMM2 tile is
 // 128 rows x 256 output columns.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -39,20 +41,77 @@ __device__ __forceinline__ uint8_t* align_1024_mk(uint8_t* p) {
 
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
 constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
-constexpr int MEGA_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+constexpr int MEGA_SMEM_BYTES = STAGES * STAGE_STRIDE + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+
+// ------------------------------------------------------------------ MXFP8 helpers
+// byte offset of (row r of a 128-row block, K-block kb of a 128-wide K step)
+// inside its 512-byte scale block
+__device__ __forceinline__ int sf_offset(int r, int kb) { return (r & 31) * 16 + ((r >> 5) & 3) * 4 + kb; }
 
 // ------------------------------------------------------------------ gather (dispatch)
-// Ring slot m % slots receives schedule rows [m b, min((m+1) b, R)) of x.
-__device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
-  const int g = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+// Ring slot m % slots receives schedule rows [m b, min((m+1) b, R)) of x, at
+// ring row (row - m b).  Gather CTA g takes the minibatch's M-tiles g, g + G,
+// ...; its warps take the tile's rows.  MXFP8: each row is quantised on the
+// way (E4M3 codes into the ring, E8M0 scales into the tile's scale blocks).
+__device__ void gather_copy_row(const FwdParams& p, const bf16* src_row, bf16* dst_row) {
+  const int lane = threadIdx.x & 31;
   const int nv = p.D / 8;  // 16-byte vectors per row
   // a whole row in flight per warp (D <= 8192 in one pass), loads before stores
   constexpr int UNR = 32;
+  const uint4* src = reinterpret_cast<const uint4*>(src_row);
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+  for (int base = 0; base < nv; base += 32 * UNR) {
+    uint4 v[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) v[u] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) dst[i] = v[u];
+    }
+  }
+}
+
+__device__ void gather_quantize_row(const FwdParams& p, const bf16* src_row, uint8_t* dst_row, uint8_t* sf_tile,
+                                    int r_in_tile) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = p.D / 32;  // lane l takes 32-element blocks l, l + 32, ...
+#pragma unroll 2
+  for (int blk = lane; blk < nblk + (32 - nblk % 32) % 32; blk += 32) {
+    const bool on = blk < nblk;
+    float v[32];
+    if (on) {
+      load_bf16x32(src_row + blk * 32, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    uint32_t q[8];
+    const uint32_t code = mx_quantize32(v, q);
+    if (on) {
+      uint4* dst = reinterpret_cast<uint4*>(dst_row + blk * 32);
+      dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    }
+    // four consecutive lanes hold the four K-blocks of one 128-wide K step
+    uint32_t word = code << (8 * (blk & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (on && (blk & 3) == 0)
+      *reinterpret_cast<uint32_t*>(sf_tile + (size_t)(blk >> 2) * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = word;
+  }
+}
+
+__device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
+  const int g = blockIdx.x;
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int m = 0; m < p.n_mb; ++m) {
     if (m >= p.slots) {
       if (threadIdx.x == 0) {
-        const int need = p.meta[META_MB + 2 * (m - p.slots)];
+        const int need = p.meta[META_MB + 4 * (m - p.slots)];
         TRACE_T0();
         *s_flag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), need, p.status, p.timeout_ns) ? 1 : 0;
         TRACE_ADD(p, TR_GATHER_WAIT);
@@ -60,27 +119,28 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
       __syncthreads();
       if (*s_flag == 0) return;
     }
-    const int lo = m * p.b, hi = min(p.R, lo + p.b);
-    const int per = (hi - lo + p.G - 1) / p.G;
-    const int r0 = lo + g * per, r1 = min(hi, r0 + per);
+    const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
     TRACE_T0();
-    for (int r = r0 + warp; r < r1; r += nwarps) {
-      const int t = p.sched[(size_t)r * 3];
-      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.D);
-      uint4* dst = reinterpret_cast<uint4*>(p.ring_x + (slot_base + (size_t)(r - lo)) * p.D);
-      for (int base = 0; base < nv; base += 32 * UNR) {
-        uint4 v[UNR];
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-          const int i = base + u * 32 + lane;
-          if (i < nv) v[u] = __ldg(src + i);
+    if (p.mx) {  // whole M-tiles per CTA: a tile's scale blocks are written by one CTA
+      const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
+      for (int i = g; i < ntile; i += p.G) {
+        const int mt = mt0 + i;
+        const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
+        for (int r = warp; r < rows; r += nwarps) {
+          const int t = p.sched[(size_t)(p0 + r) * 3];
+          const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
+          gather_quantize_row(p, p.x + (size_t)t * p.D, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
+                              p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
         }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-          const int i = base + u * 32 + lane;
-          if (i < nv) dst[i] = v[u];
-        }
+      }
+    } else {  // contiguous row ranges per CTA, rows strided over its warps
+      const int hi = min(p.R, lo + p.b);
+      const int per = (hi - lo + p.G - 1) / p.G;
+      const int r0 = lo + g * per, r1 = min(hi, r0 + per);
+      for (int r = r0 + warp; r < r1; r += nwarps) {
+        const int t = p.sched[(size_t)r * 3];
+        gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + (slot_base + (size_t)(r - lo)) * p.D);
       }
     }
     fence_proxy_async_global();
@@ -101,16 +161,21 @@ struct Operands {
   int nk;
 };
 
+__device__ __forceinline__ bool task_is_mx(const FwdParams& p, int kind) {
+  return p.mx && (kind == TASK_R1 || kind == TASK_R2);
+}
+
 __device__ __forceinline__ Operands task_operands(const TensorMaps& maps, const FwdParams& p, const Task& t) {
   Operands o;
+  const int kstep = p.mx ? BK_MX : BK;  // routed tensor maps are E4M3 (MXFP8) or bf16
   switch (t.kind) {
     case TASK_R1:
       o.a = &maps.ring_x; o.b0 = &maps.w_up; o.b1 = &maps.w_gate;
-      o.b_row = t.e * p.I + t.n * BN_UP; o.nk = p.D / BK;
+      o.b_row = t.e * p.I + t.n * BN_UP; o.nk = p.D / kstep;
       break;
     case TASK_R2:
       o.a = &maps.ring_h; o.b0 = &maps.w_down; o.b1 = nullptr;
-      o.b_row = t.e * p.D + t.n * BN_DOWN; o.nk = p.I / BK;
+      o.b_row = t.e * p.D + t.n * BN_DOWN; o.nk = p.I / kstep;
       break;
     case TASK_S1:
       o.a = &maps.x; o.b0 = &maps.ws_up; o.b1 = &maps.ws_gate;
@@ -125,7 +190,25 @@ __device__ __forceinline__ Operands task_operands(const TensorMaps& maps, const 
 }
 
 __device__ __forceinline__ int task_nk(const FwdParams& p, int kind) {
-  return (kind == TASK_R1 || kind == TASK_S1) ? p.D / BK : (kind == TASK_R2 ? p.I / BK : p.I_s / BK);
+  const int kstep = task_is_mx(p, kind) ? BK_MX : BK;
+  return (kind == TASK_R1 || kind == TASK_S1) ? p.D / kstep : (kind == TASK_R2 ? p.I / kstep : p.I_s / BK);
+}
+
+// MXFP8 scale blocks of a K step: A (the tile's rows), then B's two 128-row halves
+__device__ __forceinline__ void mx_scale_sources(const FwdParams& p, const Task& t, int kb, const uint8_t** src) {
+  if (t.kind == TASK_R1) {
+    const int nkg = p.D / BK_MX;
+    src[0] = p.sfx + ((size_t)t.mt * nkg + kb) * SF_BLOCK_BYTES;
+    const size_t wb = ((size_t)(t.e * p.I + t.n * BN_UP) / BM * nkg + kb) * SF_BLOCK_BYTES;
+    src[1] = p.w_up_sf + wb;
+    src[2] = p.w_gate_sf + wb;
+  } else {
+    const int nkg = p.I / BK_MX;
+    src[0] = p.sfh + ((size_t)t.mt * nkg + kb) * SF_BLOCK_BYTES;
+    const size_t rb = (size_t)(t.e * p.D + t.n * BN_DOWN) / BM;
+    src[1] = p.w_down_sf + (rb * nkg + kb) * SF_BLOCK_BYTES;
+    src[2] = p.w_down_sf + ((rb + 1) * nkg + kb) * SF_BLOCK_BYTES;
+  }
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -169,6 +252,20 @@ __device__ __forceinline__ uint2 pack_bf16x4(float4 f) {
   return make_uint2(pack_bf16x2(f.x, f.y), pack_bf16x2(f.z, f.w));
 }
 
+// staging rows are fp16: 10 mantissa bits keep the weighted sum's error below
+// the bf16 output rounding; values saturate at the fp16 maximum (no infinities)
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float a, float b) {
+  const float m = 65504.0f;
+  __half2 h = __floats2half2_rn(fminf(fmaxf(a, -m), m), fminf(fmaxf(b, -m), m));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float4 load_f16x4(const __half* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // up/gate tile -> h = SiLU(gate) * up (bf16): TMEM columns [0,128) up, [128,256) gate.
 // dst: row 0 of the warp's rows, column 0 of the tile; ld: row stride (elements).
 __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t ld, int nrows, uint64_t* tempty) {
@@ -196,8 +293,42 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
   }
 }
 
-// routed down-projection tile -> fp32 staging rows Y[j] (j from the schedule table)
-__device__ void epilogue_copy_f32(uint32_t taddr, EpiStage& st, float* Y, size_t D, int col0, int j_mine, int nrows,
+// MXFP8 up/gate tile -> h quantised per 32 columns: E4M3 codes into the h ring
+// (thread = row, 128 bytes) and one 32-bit word of four E8M0 codes into the
+// tile's scale block (this tile's 128 columns are one 128-wide K step of the
+// down projection).  The accumulator is handed back after the last TMEM read.
+__device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf_block, int row, bool valid,
+                                   uint64_t* tempty) {
+  uint32_t q[4][8];
+  uint32_t scales = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t u[32], g[32];
+    tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), u);
+    tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + 32 * c), g);
+    tmem_ld_wait();
+    if (c == 3) {
+      tc_fence_before();
+      mbar_arrive(tempty);
+    }
+    float h[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) h[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+    scales |= mx_quantize32(h, q[c]) << (8 * c);
+  }
+  if (valid) {
+    uint4* d = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      d[2 * c] = make_uint4(q[c][0], q[c][1], q[c][2], q[c][3]);
+      d[2 * c + 1] = make_uint4(q[c][4], q[c][5], q[c][6], q[c][7]);
+    }
+    *reinterpret_cast<uint32_t*>(sf_block + sf_offset(row, 0)) = scales;
+  }
+}
+
+// routed down-projection tile -> fp16 staging rows Y[j] (j from the schedule table)
+__device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, size_t D, int col0, int j_mine, int nrows,
                                   uint64_t* tempty) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -217,7 +348,11 @@ __device__ void epilogue_copy_f32(uint32_t taddr, EpiStage& st, float* Y, size_t
     for (int i = 0; i < 8; ++i) {
       const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
       const int jr = __shfl_sync(0xffffffffu, j_mine, rr);
-      if (rr < nrows) *reinterpret_cast<float4*>(Y + (size_t)jr * D + col0 + c + cc) = staged4(st, rr, cc);
+      if (rr < nrows) {
+        const float4 f = staged4(st, rr, cc);
+        *reinterpret_cast<uint2*>(Y + (size_t)jr * D + col0 + c + cc) = make_uint2(pack_f16x2_sat(f.x, f.y),
+                                                                                   pack_f16x2_sat(f.z, f.w));
+      }
     }
     __syncwarp();
   }
@@ -229,14 +364,13 @@ __device__ void epilogue_copy_f32(uint32_t taddr, EpiStage& st, float* Y, size_t
 // shared expert's down-projection epilogue and starts from its fp32 output;
 // without one, this pass runs once every routed output row is stored.
 __device__ __forceinline__ void accumulate_routed(const FwdParams& p, int t, int col, const float* g, float* acc) {
-  const float* y = p.Y + (size_t)t * p.k * p.D + col;
+  const __half* y = p.Y + (size_t)t * p.k * p.D + col;
 #pragma unroll
   for (int s = 0; s < TOPK_MAX; ++s) {
     if (s < p.k) {
-      const float4* src = reinterpret_cast<const float4*>(y + (size_t)s * p.D);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 f = src[i];
+        const float4 f = load_f16x4(y + (size_t)s * p.D + 4 * i);
         acc[4 * i + 0] = fmaf(g[s], f.x, acc[4 * i + 0]);
         acc[4 * i + 1] = fmaf(g[s], f.y, acc[4 * i + 1]);
         acc[4 * i + 2] = fmaf(g[s], f.z, acc[4 * i + 2]);
@@ -261,7 +395,7 @@ __device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdP
   for (int s = 0; s < TOPK_MAX; ++s) st.g[lane][s] = (lane < nrows && s < k) ? p.topk_w[(size_t)(t0 + lane) * k + s] : 0.0f;
   // the k staging rows of a token are read once: ask L2 for them two chunks
   // ahead (lane = row; one 128-byte line per slot and chunk)
-  const float* yrow = p.Y + (size_t)(t0 + lane) * k * p.D + col0;
+  const __half* yrow = p.Y + (size_t)(t0 + lane) * k * p.D + col0;
   auto prefetch_chunk = [&](int c) {
     if (lane < nrows && c < BN_DOWN)
       for (int s = 0; s < k; ++s) prefetch_l2(yrow + (size_t)s * p.D + c);
@@ -288,12 +422,12 @@ __device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdP
       if (rr < nrows) {
         const int t = t0 + rr;
         float4 acc = staged4(st, rr, cc);
-        const float* y = p.Y + (size_t)t * k * p.D + col0 + c + cc;
+        const __half* y = p.Y + (size_t)t * k * p.D + col0 + c + cc;
 #pragma unroll
         for (int s = 0; s < TOPK_MAX; ++s) {
           if (s < k) {
             const float gs = st.g[rr][s];
-            const float4 f = __ldcs(reinterpret_cast<const float4*>(y + (size_t)s * p.D));
+            const float4 f = load_f16x4(y + (size_t)s * p.D);
             acc.x = fmaf(gs, f.x, acc.x);
             acc.y = fmaf(gs, f.y, acc.y);
             acc.z = fmaf(gs, f.z, acc.z);
@@ -328,7 +462,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
     moe_megakernel(const __grid_constant__ TensorMaps maps, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024_mk(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_STRIDE);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -337,7 +471,9 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = s_flag + 1;
-  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + STAGES * STAGE_BYTES + 256);
+  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + STAGES * STAGE_STRIDE + 256);
+  // MXFP8 needs TMEM columns for the scales: one accumulator buffer instead of two
+  const uint32_t n_acc = p.mx ? 1u : 2u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
@@ -372,60 +508,132 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-      // ---------------- TMA producer
-      if (elect_one()) {
+      // ---------------- TMA producer (whole warp: lane 0 waits, loads B and
+      // arrives; with direct dispatch every lane also gathers 4 of the tile's
+      // 128 token rows per K step, and for MXFP8 writes their scale words)
+      const bool leader = lane == 0;
+      if (leader) {
         prefetch_tensormap(&maps.x);
         prefetch_tensormap(&maps.ring_x);
         prefetch_tensormap(&maps.w_up);
         prefetch_tensormap(&maps.w_gate);
         prefetch_tensormap(&maps.ring_h);
         prefetch_tensormap(&maps.w_down);
-        uint32_t stage = 0, phase = 0;
-        int issued = 0;
-        bool ok = true;
-        for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
-          const Task t = p.tasks[ti];
-          {
-            TRACE_T0();
-            if (t.dep0 >= 0 && !wait_counter_ge(p.counters + t.dep0, t.need0, p.status, p.timeout_ns)) break;
-            if (t.dep1 >= 0 && !wait_counter_ge(p.counters + t.dep1, t.need1, p.status, p.timeout_ns)) break;
-            TRACE_ADD(p, TR_PROD_DEP);
+        if (p.direct) prefetch_tensormap(&maps.x_rows);
+      }
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
+        const Task t = p.tasks[ti];
+        int good = 1;
+        if (leader) {
+          TRACE_T0();
+          if (t.dep0 >= 0 && !wait_counter_ge(p.counters + t.dep0, t.need0, p.status, p.timeout_ns)) good = 0;
+          if (good && t.dep1 >= 0 && !wait_counter_ge(p.counters + t.dep1, t.need1, p.status, p.timeout_ns)) good = 0;
+          TRACE_ADD(p, TR_PROD_DEP);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+        fence_proxy_async_global();
+        const Operands o = task_operands(maps, p, t);
+        const bool mx = task_is_mx(p, t.kind);
+        const bool gather_a = p.direct && t.kind == TASK_R1;
+        // direct dispatch: lane l fetches tile rows 4l .. 4l+3 (rows past the
+        // tile's end repeat its first token: discarded rows, in-bounds reads)
+        int tok[4] = {0, 0, 0, 0};
+        uint32_t sfw[4][4];  // MXFP8: scale words of the 4 rows, 4 K steps ahead
+        const int nkg = p.D / BK_MX;
+        if (gather_a) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 4 * lane + j;
+            tok[j] = p.sched[(size_t)(t.p0 + (r < t.rows ? r : 0)) * 3];
           }
-          fence_proxy_async_global();
-          const Operands o = task_operands(maps, p, t);
-          for (int kb = 0; kb < o.nk; ++kb) {
-            {
-              TRACE_T0();
-              if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns)) { ok = false; break; }
-              TRACE_ADD(p, TR_PROD_EMPTY);
-            }
-            uint8_t* sa = smem + stage * STAGE_BYTES;
-            uint8_t* sb = sa + A_STAGE_BYTES;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)STAGE_BYTES);
-            tma_load_2d(sa, o.a, &full[stage], kb * BK, t.a_row);
-            if (o.b1) {
-              tma_load_2d(sb, o.b0, &full[stage], kb * BK, o.b_row);
-              tma_load_2d(sb + B_STAGE_BYTES / 2, o.b1, &full[stage], kb * BK, o.b_row);
-            } else {
-              tma_load_2d(sb, o.b0, &full[stage], kb * BK, o.b_row);
-            }
-            ++issued;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (mx) {
+#pragma unroll
+            for (int d = 0; d < 4; ++d)
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                sfw[d][j] = d < o.nk ? *reinterpret_cast<const uint32_t*>(p.xs + (size_t)tok[j] * (nkg * 4) + d * 4) : 0u;
           }
         }
-        // the last STAGES loads this thread issued have landed before the CTA may exit
+        for (int kb = 0; kb < o.nk; ++kb) {
+          int free = 1;
+          if (leader) {
+            TRACE_T0();
+            free = mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns) ? 1 : 0;
+            TRACE_ADD(p, TR_PROD_EMPTY);
+          }
+          if (!__shfl_sync(0xffffffffu, free, 0)) { ok = false; break; }
+          uint8_t* sa = smem + stage * STAGE_STRIDE;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          uint8_t* ssf = sa + STAGE_BYTES;
+          // a K step is 64 bf16 or 128 E4M3 elements: 128 bytes per row either way
+          const int kc = kb * (mx ? BK_MX : BK);
+          if (gather_a) {
+            tma_gather4(sa + lane * 4 * 128, &maps.x_rows, &full[stage], kc, tok[0], tok[1], tok[2], tok[3]);
+            if (mx) {  // the tile's A scale block, written here rather than copied
+              const int d = kb & 3;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int dd = 0; dd < 4; ++dd)
+                  if (dd == d) w = sfw[dd][j];
+                *reinterpret_cast<uint32_t*>(ssf + sf_offset(4 * lane + j, 0)) = w;
+              }
+              if (kb + 4 < o.nk) {  // refill this slot with K step kb + 4
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint32_t w = *reinterpret_cast<const uint32_t*>(p.xs + (size_t)tok[j] * (nkg * 4) + (kb + 4) * 4);
+#pragma unroll
+                  for (int dd = 0; dd < 4; ++dd)
+                    if (dd == d) sfw[dd][j] = w;
+                }
+              }
+              fence_proxy_async_smem();
+            }
+          }
+          __syncwarp();
+          if (leader) {
+            // bytes the TMA engine delivers (the scale block written above is not counted)
+            const uint32_t tx = (mx ? (uint32_t)MX_STAGE_TX : (uint32_t)STAGE_BYTES) -
+                                (gather_a && mx ? (uint32_t)SF_BLOCK_BYTES : 0u);
+            mbar_arrive_expect_tx(&full[stage], tx);
+            if (!gather_a) tma_load_2d(sa, o.a, &full[stage], kc, t.a_row);
+            if (o.b1) {
+              tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
+              tma_load_2d(sb + B_STAGE_BYTES / 2, o.b1, &full[stage], kc, o.b_row);
+            } else {
+              tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
+            }
+            if (mx) {
+              const uint8_t* src[3];
+              mx_scale_sources(p, t, kb, src);
+              for (int i = gather_a ? 1 : 0; i < 3; ++i)
+                bulk_load(ssf + i * SF_BLOCK_BYTES, src[i], SF_BLOCK_BYTES, &full[stage]);
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // the last STAGES loads this warp issued have landed before the CTA may exit
+      if (leader)
         for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
           mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, p.status, p.timeout_ns);
-      }
       __syncwarp();
     } else if (warp == 1) {
       // ---------------- MMA issuer
       if (elect_one()) {
         const uint32_t idesc = idesc_bf16_f32(BM, 256);
+        const uint32_t idesc_mx = idesc_mxf8_e4m3(BM, 256);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
         for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
-          const int nk = task_nk(p, p.tasks[ti].kind);
+          const int kind = p.tasks[ti].kind;
+          const bool mx = task_is_mx(p, kind);
+          const int nk = task_nk(p, kind);
           {
             TRACE_T0();
             if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.status, p.timeout_ns)) break;
@@ -440,18 +648,31 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
               TRACE_ADD(p, TR_MMA_FULL);
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t a_addr = smem_u32(smem + stage * STAGE_STRIDE);
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+            if (mx) {
+              // scales -> TMEM (in order with the MMAs below), then four 32-wide K blocks
+              const uint32_t sf = a_addr + STAGE_BYTES;
+              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
+              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
+              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
 #pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_mxf8_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
+                            idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
+                            tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                            (kb | kk) != 0 ? 1u : 0u);
+            }
             mma_commit(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
           mma_commit(&tfull[acc]);
-          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+          if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
         }
         mma_commit(drain);
         mbar_wait(drain, 0, p.status, p.timeout_ns);
@@ -484,14 +705,18 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         const int r0 = q * 32;                        // the warp's first tile row
         const int nrows = min(32, max(0, t.rows - r0));  // its valid rows
         EpiStage& st = epi[q];
-        if (t.kind == TASK_R1) {
+        if (t.kind == TASK_R1 && p.mx) {
+          epilogue_swiglu_mx(taddr, reinterpret_cast<uint8_t*>(p.ring_h) + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
+                             p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows,
+                             &tempty[acc]);
+        } else if (t.kind == TASK_R1) {
           epilogue_swiglu(taddr, st, p.ring_h + (size_t)(t.out_row + r0) * p.I + t.n * BN_UP, p.I, nrows, &tempty[acc]);
         } else if (t.kind == TASK_S1) {
           epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows,
                           &tempty[acc]);
         } else if (t.kind == TASK_R2) {
           const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
-          epilogue_copy_f32(taddr, st, p.Y, p.D, t.n * BN_DOWN, j, nrows, &tempty[acc]);
+          epilogue_copy_f16(taddr, st, p.Y, p.D, t.n * BN_DOWN, j, nrows, &tempty[acc]);
         } else {
           epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, &tempty[acc]);
         }
@@ -505,7 +730,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
           if (t.done0 >= 0) red_release_add_gpu(p.counters + t.done0, 1);
           if (t.done1 >= 0) red_release_add_gpu(p.counters + t.done1, 1);
         }
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
       }
     }
     tc_fence_before();

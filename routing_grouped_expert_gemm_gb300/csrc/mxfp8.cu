@@ -3,7 +3,10 @@
 // Format: OCP Microscaling (MX) v1.0, MXFP8 E4M3, one E8M0 scale per 32
 // consecutive elements along K:  X = 2^(floor(log2 amax) - 8)  (8 = exponent of
 // E4M3's largest normal, 448), q = E4M3_rne_satfinite(v / X); amax = 0 -> X = 2^-127.
-// Scale layout: [rows, K/32] row-major bytes.
+// Scale layout (what the block-scaled MMA loads with tcgen05.cp): 512-byte
+// blocks, one per 128 rows x 128 K-elements, ordered [rows/128][K/128]; inside
+// a block the scale of row r (mod 128) and 32-wide K block kb (mod 4) is at
+// byte (r % 32) * 16 + (r / 32) * 4 + kb.  rows and K are multiples of 128.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -57,8 +60,39 @@ __global__ void mx_quantize_kernel(const bf16* __restrict__ W, int64_t rows, int
     uint4* dst = reinterpret_cast<uint4*>(q + r * K + b * 32);
     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    scales[r * nb + b] = code;
+    const int64_t sblk = (r / 128) * (K / 128) + b / 4;
+    scales[sblk * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4)] = code;
   }
+}
+
+// Activation quantisation for direct dispatch (Sec. 3.4: activation
+// quantisation is fused into the dispatch): every token row of x is quantised
+// once, whatever the number of experts it goes to.  One warp per row, lane l
+// takes the 32-element blocks l, l + 32, ...; codes [T, D], scales [T, D/32].
+__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const bf16* __restrict__ x, int T, int D,
+                                                                uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = D / 32;
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += gridDim.x * (blockDim.x >> 5)) {
+#pragma unroll 2
+    for (int blk = lane; blk < nblk; blk += 32) {
+      float v[32];
+      load_bf16x32(x + (size_t)t * D + blk * 32, v);
+      uint32_t q[8];
+      const uint32_t code = mx_quantize32(v, q);
+      uint4* dst = reinterpret_cast<uint4*>(xq + (size_t)t * D + blk * 32);
+      dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      xs[(size_t)t * nblk + blk] = (uint8_t)code;
+    }
+  }
+}
+
+cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st) {
+  int grid = (T + 7) / 8;
+  if (grid > 152 * 8) grid = 152 * 8;
+  mx_quantize_rows_kernel<<<grid, 256, 0, st>>>(x, T, D, xq, xs);
+  return cudaGetLastError();
 }
 
 size_t mx_scale_bytes(int64_t rows, int64_t K) { return (size_t)(rows * (K / 32)); }

@@ -78,7 +78,7 @@ RouteLayout route_layout(int64_t T, int64_t E, int64_t k) {
   };
   L.status = take(sizeof(int));
   L.counters = take(sizeof(int) * (size_t)L.n_counters);
-  L.meta = take(sizeof(int) * (size_t)(META_MB + 2 * L.n_mb));
+  L.meta = take(sizeof(int) * (size_t)(META_MB + 4 * L.n_mb));
   L.chunk_counts = take(sizeof(int) * (size_t)L.n_chunks * (size_t)E);
   L.mtiles = take(sizeof(int) * 4 * (size_t)L.n_mtiles_max);
   L.segs = take(sizeof(int) * (size_t)(4 * L.max_segs + 4 * (2 * L.max_segs + 2) + L.n_mb + 1));

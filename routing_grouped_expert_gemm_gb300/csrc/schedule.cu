@@ -122,8 +122,9 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
 //   S2 (shared expert down projection + combine, all tokens)
 // R1(m) / R2(m): for each segment of minibatch m (an expert's rows inside m),
 // for each column tile n, for each M-tile of the segment -- the M-tiles that
-// share a weight slice run side by side (slice read from HBM once) and a
-// segment's A rows stay in L2 across its column tiles.
+// share a weight slice run side by side (slice read from HBM once).
+// S1 / S2: token-tile major -- the column tiles of one token tile run side by
+// side, so the combine in S2 reads whole staging rows at once.
 // A GEMM CTA takes tasks g, g + n_gemm, g + 2 n_gemm, ...; every dependency of
 // a task points to an earlier task (or to the gather, whose own dependencies
 // are earlier tasks), so the smallest unfinished task can always proceed.
@@ -245,8 +246,10 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   // per-minibatch task counts and the first task of every step
   if (blockIdx.x == 0) {
     for (int m = tid; m < n_mb; m += blockDim.x) {
-      p.meta[META_MB + 2 * m] = fits ? mb_tiles[m] * p.N1 : 0;
-      p.meta[META_MB + 2 * m + 1] = fits ? mb_tiles[m] * p.N2 : 0;
+      p.meta[META_MB + 4 * m] = fits ? mb_tiles[m] * p.N1 : 0;
+      p.meta[META_MB + 4 * m + 1] = fits ? mb_tiles[m] * p.N2 : 0;
+      p.meta[META_MB + 4 * m + 2] = fits ? mt_first[m] : 0;
+      p.meta[META_MB + 4 * m + 3] = fits ? mb_tiles[m] : 0;
     }
   }
   for (int s = tid; s < n_steps; s += blockDim.x) {
@@ -277,10 +280,11 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   for (int q = blockIdx.x * blockDim.x + tid; q < n_s1 + n_s2; q += gridDim.x * blockDim.x) {
     const bool down = q >= n_s1;
     const int qq = down ? q - n_s1 : q;
-    const int mt = qq % p.n_smtiles;
+    const int nn = down ? p.N2s : p.N1s;
+    const int mt = qq / nn;  // token-tile major, as for the routed segments
     Task tk;
     tk.kind = down ? TASK_S2 : TASK_S1;
-    tk.n = qq / p.n_smtiles;
+    tk.n = qq % nn;
     tk.e = 0;
     tk.a_row = mt * BM;
     tk.rows = min(BM, p.T - mt * BM);
@@ -292,7 +296,8 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
     tk.need1 = 0;
     tk.done0 = down ? -1 : ctr_shready(p, mt);
     tk.done1 = -1;
-    tk.pad[0] = tk.pad[1] = tk.pad[2] = 0;
+    tk.mt = mt;
+    tk.pad[0] = tk.pad[1] = 0;
     store_task(p.tasks + (down ? (int)total - n_s2 + qq : qq), tk);
   }
   // routed tasks: CTA c fills experts c, c + gridDim.x, ...; its threads stride
@@ -314,7 +319,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
       for (int q = tid; q < cnt * (p.N1 + p.N2); q += blockDim.x) {
         const bool down = q >= cnt * p.N1;
         const int qq = down ? q - cnt * p.N1 : q;
-        const int i = qq % cnt;
+        const int i = qq % cnt;  // column-tile major: the segment's tiles share a weight slice
         const int r0 = a + i * BM;
         Task tk;
         tk.kind = down ? TASK_R2 : TASK_R1;
@@ -325,7 +330,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
         tk.p0 = r0;
         tk.out_row = tk.a_row;
         if (!down) {
-          tk.dep0 = ctr_filled(p, m);
+          tk.dep0 = p.direct ? -1 : ctr_filled(p, m);  // direct dispatch: x itself is the A operand
           tk.need0 = p.G;
           tk.dep1 = m >= p.slots ? ctr_r2(p, m - p.slots) : -1;
           tk.need1 = need_h;
@@ -339,8 +344,16 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           tk.done0 = ctr_r2(p, m);
           tk.done1 = ctr_ydone();
         }
-        tk.pad[0] = tk.pad[1] = tk.pad[2] = 0;
+        tk.mt = mtb + i;
+        tk.pad[0] = tk.pad[1] = 0;
         store_task(p.tasks + (down ? r2_base : r1_base) + qq, tk);
+      }
+      for (int i = tid; i < cnt; i += blockDim.x) {  // the M-tile table (the gather walks it)
+        int* mr = p.mtiles + 4 * (mtb + i);
+        mr[0] = e;
+        mr[1] = a + i * BM;
+        mr[2] = min(BM, z - (a + i * BM));
+        mr[3] = m;
       }
       mtb += cnt;
     }

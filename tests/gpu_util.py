@@ -24,7 +24,8 @@ class Layer:
         s = inp.shape
         self.shape = s
         self.T_max = T_max or inp.T
-        self.plan = rg.moe_plan_create(self.T_max, s.D, s.I, s.E, s.k, s.I_s, score_fn=s.score, **plan_kw)
+        self.plan = rg.moe_plan_create(self.T_max, s.D, s.I, s.E, s.k, s.I_s, score_fn=s.score,
+                                       precision=s.precision, **plan_kw)
         self.w = {
             "W_router": to_dev_bf16(inp.w_router),
             "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).to("cuda"),
@@ -32,6 +33,15 @@ class Layer:
             "W_gate": to_dev_bf16(inp.w_gate),
             "W_down": to_dev_bf16(inp.w_down),
         }
+        self.mx = s.precision == "mxfp8"
+        if self.mx:  # routed weights quantised on the GPU (codes + scale blocks)
+            self.w_bf16 = {k: self.w[k] for k in ("W_up", "W_gate", "W_down")}
+            for name, rows, K in (("W_up", s.E * s.I, s.D), ("W_gate", s.E * s.I, s.D), ("W_down", s.E * s.D, s.I)):
+                q = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+                sc = torch.empty(rg.moe_mxfp8_scale_bytes(rows, K), dtype=torch.uint8, device="cuda")
+                rg.moe_quantize_mxfp8(self.plan, self.w[name], rows, K, q, sc)
+                self.w[name] = q
+                self.w[name + "_scale"] = sc
         if shared and s.I_s > 0:
             self.w.update(Ws_up=to_dev_bf16(inp.ws_up), Ws_gate=to_dev_bf16(inp.ws_gate),
                           Ws_down=to_dev_bf16(inp.ws_down))
@@ -74,3 +84,9 @@ def check_out(gpu: np.ndarray, ref: np.ndarray, rel_tol: float = 1e-2, maxabs_fr
     assert rel <= rel_tol, f"rel-L2 {rel:.3g} > {rel_tol}"
     assert mabs <= maxabs_frac * rms, f"max-abs {mabs:.3g} > {maxabs_frac} * rms {rms:.3g}"
     return rel, mabs / rms
+
+
+def scale_blocks_to_rows(blocks: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Library scale layout (512-byte blocks [rows/128][K/128]) -> [rows, K/32]."""
+    b = blocks.reshape(rows // 128, K // 128, 32, 4, 4)  # [rb, kg, r%32, (r%128)//32, kb]
+    return b.transpose(0, 3, 2, 1, 4).reshape(rows, K // 32)

@@ -63,19 +63,21 @@ def run_and_check(inp, T=None, **plan_kw):
     return layer, x, res
 
 
-def test_tiny_workload_all_tokens():
-    run_and_check(mi.make_inputs("tiny"), minibatch=512, ring_slots=2, gather_ctas=2)
+@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+def test_tiny_workload_all_tokens(dispatch):
+    run_and_check(mi.make_inputs("tiny"), minibatch=512, ring_slots=2, gather_ctas=2, dispatch=dispatch)
 
 
-def test_medium_ragged_tokens_and_tiles():
+@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+def test_medium_ragged_tokens_and_tiles(dispatch):
     # 1000 tokens: ragged 128-token tail, several column tiles, partial M-tiles per expert
-    run_and_check(small(1000, 512, 256, 32, 6, 256), minibatch=1024, ring_slots=3, gather_ctas=4)
+    run_and_check(small(1000, 512, 256, 32, 6, 256), minibatch=1024, ring_slots=3, gather_ctas=4, dispatch=dispatch)
 
 
-@pytest.mark.parametrize("T", [1, 127, 129])
-def test_edge_token_counts(T):
+@pytest.mark.parametrize("T,dispatch", [(1, "ring"), (127, "ring"), (129, "ring"), (1, "direct"), (129, "direct")])
+def test_edge_token_counts(T, dispatch):
     inp = small(256, 256, 128, 16, 4, 128, cid=301)
-    run_and_check(inp, T=T, minibatch=128, ring_slots=2, gather_ctas=1)
+    run_and_check(inp, T=T, minibatch=128, ring_slots=2, gather_ctas=1, dispatch=dispatch)
 
 
 def test_no_shared_expert_softmax():
@@ -118,7 +120,9 @@ def test_bitwise_deterministic_across_knobs():
                dict(minibatch=128, ring_slots=2, gather_ctas=1, lag=1),
                dict(minibatch=256, ring_slots=1, gather_ctas=8, lag=0),
                dict(minibatch=8192, ring_slots=1, gather_ctas=2, lag=0, gemm_ctas=20),
-               dict(minibatch=512, ring_slots=5, gather_ctas=16, lag=1, gemm_ctas=7)):
+               dict(minibatch=512, ring_slots=5, gather_ctas=16, lag=1, gemm_ctas=7),
+               dict(minibatch=1024, ring_slots=3, dispatch="direct"),
+               dict(minibatch=128, ring_slots=1, lag=0, dispatch="direct", gemm_ctas=11)):
         layer = g.Layer(inp, **kw)
         res = layer.run(x, poison=True)
         assert res["status"] == 0
@@ -146,9 +150,10 @@ def _full_size(name, n_sample=48, **plan_kw):
     return g.check_out(got, ref)
 
 
-def test_full_size_dsv3_zipf_sampled():
-    _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8)
+@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+def test_full_size_dsv3_zipf_sampled(dispatch):
+    _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8, dispatch=dispatch)
 
 
 def test_full_size_qwen3_sampled():
-    _full_size("qwen3", minibatch=4096, ring_slots=4, gather_ctas=8)
+    _full_size("qwen3", minibatch=4096, ring_slots=4, gather_ctas=8, dispatch="direct")
