@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 sub-measurement")
+    ap.add_argument("--gather-ctas-mx", type=int, default=12, help="gather CTAs for the MXFP8 layer")
+    ap.add_argument("--dispatch", choices=["ring", "direct"], default="ring")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: a smaller case with this many tokens (uniform routing)")
     ap.add_argument("--experts", type=int, default=0,
@@ -73,7 +76,7 @@ def select_workload(args):
     T = args.tokens or shape.T
     E = args.experts or shape.E
     small = mi.custom_shape(T, shape.D, shape.I, E, shape.k, shape.I_s, score=shape.score,
-                            config_id=shape.config_id + 1000)
+                            config_id=shape.config_id + 1000, precision=shape.precision)
     return small, mi.make_inputs(small, calibration={"beta": None, "redraw": {}})
 
 
@@ -203,7 +206,7 @@ def workload_config(shape, args, extra=None):
            "T": shape.T, "D": shape.D, "I": shape.I, "E": shape.E, "k": shape.k, "I_s": shape.I_s,
            "score": shape.score, "load": "Zipf(1.1) via router bias" if shape.load == "zipf" else shape.load,
            "precision": shape.precision, "minibatch": args.minibatch, "ring_slots": args.ring_slots,
-           "gather_ctas": args.gather_ctas, "lag": args.lag,
+           "gather_ctas": args.gather_ctas, "lag": args.lag, "dispatch": args.dispatch,
            "l2": "inputs larger than L2 (expert weights 22.5 GB, x 235 MB for dsv3); no flush",
            "parallelism": "replicas"}
     if extra:
@@ -212,6 +215,116 @@ def workload_config(shape, args, extra=None):
 
 
 # ----------------------------------------------------------------------------- our arm
+class Runner:
+    """One workload on the device: plan, weights (MXFP8 quantised outside any
+    timed region), workspace, and a timed loop of moe_fwd calls."""
+
+    def __init__(self, rg, torch, shape, inp, args, world):
+        self.rg, self.torch, self.shape, self.inp, self.args, self.world = rg, torch, shape, inp, args, world
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+        T = shape.T
+        self.plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,
+                                       precision=shape.precision, minibatch=args.minibatch,
+                                       ring_slots=args.ring_slots,
+                                       gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8"
+                                       else args.gather_ctas,
+                                       lag=args.lag, dispatch=args.dispatch)
+        w = {"W_router": dev(inp.w_router),
+             "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()}
+        for name, arr, rows, K in (("W_up", inp.w_up, shape.E * shape.I, shape.D),
+                                   ("W_gate", inp.w_gate, shape.E * shape.I, shape.D),
+                                   ("W_down", inp.w_down, shape.E * shape.D, shape.I)):
+            wd = dev(arr)
+            if shape.precision == "mxfp8":  # pre-quantised weights (MoK Sec. 3.4), not timed
+                q = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+                sc = torch.empty(rg.moe_mxfp8_scale_bytes(rows, K), dtype=torch.uint8, device="cuda")
+                rg.moe_quantize_mxfp8(self.plan, wd, rows, K, q, sc)
+                torch.cuda.synchronize()
+                del wd
+                w[name], w[name + "_scale"] = q, sc
+            else:
+                w[name] = wd
+        if shape.I_s:
+            w.update(Ws_up=dev(inp.ws_up), Ws_gate=dev(inp.ws_gate), Ws_down=dev(inp.ws_down))
+        self.w = w
+        self.x = dev(inp.x)
+        self.ws_bytes = rg.moe_workspace_bytes(self.plan, T)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty((T, shape.D), dtype=torch.bfloat16, device="cuda")
+        self.stream = torch.cuda.current_stream()
+        self.launches = 3 + (1 if shape.precision == "mxfp8" and args.dispatch == "direct" else 0)
+
+    def step(self, x=None):
+        self.rg.moe_fwd(self.plan, self.shape.T, self.x if x is None else x, self.w, self.out, self.ws,
+                        self.ws_bytes, stream=self.stream)
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def status(self):
+        return self.rg.moe_get_status(self.plan, self.ws, stream=self.stream)
+
+    def timed(self, steps, warmup, sampler=None):
+        torch, rg = self.torch, self.rg
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        if self.status() != 0:
+            raise SystemExit(f"device status {self.status()} after warm-up")
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for e4 in ev:  # torch creates the CUDA event at its first record
+            for e in e4:
+                e.record(self.stream)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        self.barrier()
+        torch.cuda.synchronize()
+        start.record(self.stream)
+        for i in range(steps):
+            rg.moe_plan_set_timing_events(self.plan, ev[i])
+            self.step()
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        self.barrier()
+        clocks = sampler.stop() if sampler else None
+        rg.moe_plan_set_timing_events(self.plan, None)
+        if self.status() != 0:
+            raise SystemExit(f"device status {self.status()} in the timed region")
+        return {"elapsed_ms": start.elapsed_time(end),
+                "router_ms": [e[0].elapsed_time(e[1]) for e in ev],
+                "sched_ms": [e[1].elapsed_time(e[2]) for e in ev],
+                "mega_ms": [e[2].elapsed_time(e[3]) for e in ev],
+                "step_ms": [e[0].elapsed_time(e[3]) for e in ev], "clocks": clocks}
+
+    def e2e(self, steps):
+        """pinned host x -> device, forward, device -> pinned host out, every step"""
+        torch = self.torch
+        x_host = torch.from_numpy(np.ascontiguousarray(self.inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+        out_host = torch.empty((self.shape.T, self.shape.D), dtype=torch.bfloat16).pin_memory()
+        x_in = torch.empty_like(self.x)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            x_in.copy_(x_host, non_blocking=True)
+            self.step(x_in)
+            out_host.copy_(self.out, non_blocking=True)
+        self.barrier()
+        torch.cuda.synchronize()
+        s0.record(self.stream)
+        for _ in range(steps):
+            x_in.copy_(x_host, non_blocking=True)
+            self.step(x_in)
+            out_host.copy_(self.out, non_blocking=True)
+        s1.record(self.stream)
+        torch.cuda.synchronize()
+        self.barrier()
+        return {"ms": s0.elapsed_time(s1), "h2d": x_host.numel() * 2, "d2h": out_host.numel() * 2}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import routing_grouped_expert_gemm_gb300 as rg
@@ -222,100 +335,7 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     rgbuild.build()
-    t_gen = time.perf_counter()
-    shape, inp = select_workload(args)
-    t_gen = time.perf_counter() - t_gen
-    if shape.precision != "bf16":
-        raise SystemExit("only the bf16 path is benchmarked by this arm")
 
-    def dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-    T = shape.T
-    plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,
-                              minibatch=args.minibatch, ring_slots=args.ring_slots, gather_ctas=args.gather_ctas,
-                              lag=args.lag)
-    w = {"W_router": dev(inp.w_router),
-         "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda(),
-         "W_up": dev(inp.w_up), "W_gate": dev(inp.w_gate), "W_down": dev(inp.w_down)}
-    if shape.I_s:
-        w.update(Ws_up=dev(inp.ws_up), Ws_gate=dev(inp.ws_gate), Ws_down=dev(inp.ws_down))
-    x = dev(inp.x)
-    ws_bytes = rg.moe_workspace_bytes(plan, T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    out = torch.empty((T, shape.D), dtype=torch.bfloat16, device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step():
-        rg.moe_fwd(plan, T, x, w, out, ws, ws_bytes, stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    status = rg.moe_get_status(plan, ws, stream=stream)
-    if status != 0:
-        raise SystemExit(f"device status {status} after warm-up")
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    # ---- device-resident timed region (per-launch events on the launching stream)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for e4 in ev:  # torch creates the CUDA event at its first record
-        for e in e4:
-            e.record(stream)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    start.record(stream)
-    for i in range(args.steps):
-        rg.moe_plan_set_timing_events(plan, ev[i])
-        step()
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop()
-    rg.moe_plan_set_timing_events(plan, None)
-    status = rg.moe_get_status(plan, ws, stream=stream)
-    if status != 0:
-        raise SystemExit(f"device status {status} in the timed region")
-    elapsed_ms = start.elapsed_time(end)
-    router_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    sched_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    mega_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-
-    # ---- end to end: pinned host x in, host out back, every step
-    e2e = None
-    if not args.no_e2e:
-        x_host = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
-        out_host = torch.empty((T, shape.D), dtype=torch.bfloat16).pin_memory()
-        x_in = torch.empty_like(x)
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for _ in range(3):
-            x_in.copy_(x_host, non_blocking=True)
-            rg.moe_fwd(plan, T, x_in, w, out, ws, ws_bytes, stream=stream)
-            out_host.copy_(out, non_blocking=True)
-        barrier()
-        torch.cuda.synchronize()
-        s0.record(stream)
-        for _ in range(args.steps):
-            x_in.copy_(x_host, non_blocking=True)
-            rg.moe_fwd(plan, T, x_in, w, out, ws, ws_bytes, stream=stream)
-            out_host.copy_(out, non_blocking=True)
-        s1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        e2e_ms = s0.elapsed_time(s1)
-        e2e = {"ms": e2e_ms, "h2d": x_host.numel() * 2, "d2h": out_host.numel() * 2}
-
-    # ---- max over ranks
     def allmax(v):
         if world == 1:
             return v
@@ -324,47 +344,85 @@ def run_ours(args, world, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    elapsed_ms = allmax(elapsed_ms)
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+
+    t_gen = time.perf_counter()
+    shape, inp = select_workload(args)
+    t_gen = time.perf_counter() - t_gen
+    run = Runner(rg, torch, shape, inp, args, world)
+    res = run.timed(args.steps, args.warmup, ClockSampler(local))
+    e2e = None if args.no_e2e else run.e2e(args.steps)
+    T = shape.T
+    elapsed_ms = allmax(res["elapsed_ms"])
     if e2e:
         e2e["ms"] = allmax(e2e["ms"])
-    if rank != 0:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return 0
-
-    peaks, peak_src = load_peaks()
     flops = shape.flops(T)
-    mega_mean = sum(mega_ms) / len(mega_ms)
+    mx_peak = 2.0 * bf16_peak  # MXFP8 dense peak = 2x BF16 (MoK Sec. 4.1; nominal 4.5 vs 2.25 PFLOP/s)
+    peak = mx_peak if shape.precision == "mxfp8" else bf16_peak
+    mega_mean = sum(res["mega_ms"]) / len(res["mega_ms"])
     achieved = flops / (mega_mean / 1000.0) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    value = world * T * args.steps / (elapsed_ms / 1000.0)
     line = {
         "metric": METRIC,
-        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, random-init weights)",
+        "value": world * T * args.steps / (elapsed_ms / 1000.0), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.precision == "bf16" else "mxfp8 (e4m3 + e8m0) routed, bf16 shared",
+        "data": "synthetic (seeded normal inputs, random-init weights)",
         "config": workload_config(shape, args),
         "tflops": world * flops * args.steps / (elapsed_ms / 1000.0) / 1e12,
-        "tflops_frac_of_peak": (world * flops * args.steps / (elapsed_ms / 1000.0) / 1e12) / (world * peak),
-        "ms_median_step": statistics.median(step_ms),
-        "phases_ms_mean": {"router_topk": sum(router_ms) / len(router_ms), "schedule": sum(sched_ms) / len(sched_ms),
-                           "megakernel": mega_mean},
+        "ms_median_step": statistics.median(res["step_ms"]),
+        "phases_ms_mean": {"router_topk": statistics.mean(res["router_ms"]),
+                           "schedule": statistics.mean(res["sched_ms"]), "megakernel": mega_mean},
         "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
-                     "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"])},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
+                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)"
+                                    + (", x2 for MXFP8" if shape.precision == "mxfp8" else ""),
+                     "frac_of_burst_peak": achieved / (float(peaks["bf16_tflops"])
+                                                       * (2.0 if shape.precision == "mxfp8" else 1.0))},
+        "gpu_launches": run.launches * args.steps,
+        "clocks": res["clocks"],
         "input_generation_s": t_gen,
     }
+    line["tflops_frac_of_peak"] = line["tflops"] / (world * peak)
     if e2e:
         line["e2e"] = {"value": world * T * args.steps / (e2e["ms"] / 1000.0), "unit": "tokens/s",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
-    if world == 1 and not args.no_cpu_baseline:
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline and rank == 0:
         cb = time_oracle(inp, args.cpu_seconds)
-        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
-    print(json.dumps(line), flush=True)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = cpu
+    del run
+    torch.cuda.empty_cache()
+
+    # the same layer in MXFP8 (routed experts), its own seeded inputs, uniform routing
+    if not args.no_mxfp8 and args.workload == "dsv3" and not (args.tokens or args.experts):
+        mshape = mi.CONFIGS["dsv3_mxfp8"]
+        minp = mi.make_inputs(mshape)
+        mrun = Runner(rg, torch, mshape, minp, args, world)
+        mres = mrun.timed(args.steps, args.warmup)
+        m_el = allmax(mres["elapsed_ms"])
+        m_mega = statistics.mean(mres["mega_ms"])
+        m_ach = mshape.flops() / (m_mega / 1000.0) / 1e12
+        line["mxfp8"] = {
+            "workload": "dsv3_mxfp8: DSV3 shape, uniform routing, routed experts MXFP8, shared expert BF16",
+            "value": world * mshape.T * args.steps / (m_el / 1000.0), "unit": "tokens/s",
+            "ms_per_step": m_el / args.steps, "tflops": world * mshape.flops() * args.steps / (m_el / 1000.0) / 1e12,
+            "gather_ctas": args.gather_ctas_mx,
+            "phases_ms_mean": {"router_topk": statistics.mean(mres["router_ms"]),
+                               "schedule": statistics.mean(mres["sched_ms"]), "megakernel": m_mega},
+            "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": m_ach, "peak": mx_peak,
+                         "unit": "TFLOP/s", "frac": m_ach / mx_peak,
+                         "peak_source": f"{peak_src} bf16 sustained x2 (MXFP8 dense = 2x BF16)"},
+            "gpu_launches": mrun.launches * args.steps,
+        }
+        del mrun
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     return 0
 
 
