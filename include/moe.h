@@ -87,6 +87,8 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe
  *   lag        0: down projections of minibatch m follow its up/gate tiles;
  *              1: they follow the up/gate tiles of minibatch m + 1
  *   timeout_ms limit of every device-side wait (0 = 2000 ms)
+ *   l2_prefetch  K steps ahead that the GEMM producers prefetch operand tiles
+ *              into L2 (0 = off, the default: on DSV3 it measured slower)
  * Zero for minibatch / ring_slots / gather_ctas / lag picks the defaults
  * (8192 / 4 / 8 / 1).
  */
@@ -106,7 +108,8 @@ typedef struct moe_config {
   int32_t lag;
   int32_t timeout_ms;
   int32_t dispatch;
-  int32_t reserved[3];
+  int32_t l2_prefetch;
+  int32_t reserved[2];
 } moe_config;
 
 /*

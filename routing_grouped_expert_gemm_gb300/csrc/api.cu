@@ -72,8 +72,8 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.ring_x = take(direct ? 0 : (size_t)ring_rows * c.D * elem);
   L.ring_h = take((size_t)ring_rows * c.I * elem);
   L.sfx = take(mx && !direct ? (size_t)L.n_mtiles_max * (c.D / BK_MX) * SF_BLOCK_BYTES : 0);
-  L.xq = take(mx && direct ? (size_t)T * c.D : 0);
-  L.xs = take(mx && direct ? (size_t)T * (c.D / 32) : 0);
+  L.xq = take(mx ? (size_t)T * c.D : 0);  // x quantised once per token (both dispatch modes)
+  L.xs = take(mx ? (size_t)T * (c.D / 32) : 0);
   L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
   L.Y = take((size_t)L.R * c.D * 2);
@@ -137,6 +137,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.ring_slots == 0) c.ring_slots = 4;
   if (c.gather_ctas == 0 && c.dispatch == MOE_DISPATCH_RING) c.gather_ctas = 8;
   if (c.timeout_ms <= 0) c.timeout_ms = 2000;
+  if (c.l2_prefetch < 0 || c.l2_prefetch > 64) return MOE_ERR_INVALID_ARG;
   if (c.lag < 0 || c.lag > 1) return MOE_ERR_INVALID_ARG;
   if (c.score_fn != MOE_SCORE_SIGMOID && c.score_fn != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID_ARG;
   if (c.precision != MOE_PREC_BF16 && c.precision != MOE_PREC_MXFP8) return MOE_ERR_INVALID_ARG;
@@ -267,6 +268,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.n_tasks_max = (int)L.n_tasks_max;
   p.n_counters = (int)L.n_counters;
   p.timeout_ns = (long long)c.timeout_ms * 1000000LL;
+  p.l2_prefetch = c.l2_prefetch;
   p.x = static_cast<const bf16*>(x);
   p.b_router = w->b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);
@@ -285,8 +287,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.ring_x = reinterpret_cast<bf16*>(ws + L.ring_x);
   p.ring_h = reinterpret_cast<bf16*>(ws + L.ring_h);
   p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
-  p.xq = mx && p.direct ? ws + L.xq : nullptr;
-  p.xs = mx && p.direct ? ws + L.xs : nullptr;
+  p.xq = mx ? ws + L.xq : nullptr;
+  p.xs = mx ? ws + L.xs : nullptr;
   p.sfh = mx ? ws + L.sfh : nullptr;
   p.w_up_sf = mx ? w->W_up_scale : nullptr;
   p.w_gate_sf = mx ? w->W_gate_scale : nullptr;
@@ -342,7 +344,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   if (pl->timed && cudaEventRecord(pl->timing[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_schedule(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (mx && p.direct && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
+  if (mx && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_megakernel(tm, p, pl->grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[3], stream) != cudaSuccess) return MOE_ERR_CUDA;

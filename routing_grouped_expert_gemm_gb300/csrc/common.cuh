@@ -79,6 +79,7 @@ struct FwdParams {
   int n_router_cols;    // E rounded up (MMA N of the router)
   int n_mtiles_max, n_smtiles, n_tasks_max;
   int n_counters;
+  int l2_prefetch;      // K steps ahead that the producer prefetches into L2 (0 = off)
   long long timeout_ns;
   // inputs
   const bf16* x;
@@ -119,15 +120,26 @@ enum : int {
   TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_EPI_R1, TR_EPI_R2, TR_EPI_S1, TR_EPI_S2,
   TRACE_SLOTS = 16
 };
+// Each thread that times anything keeps its sums in registers (TRACE_LOCALS)
+// and adds them to the CTA's slots once, at the end (TRACE_FLUSH), so the
+// timers stay off the paths they measure.
 #ifdef MOE_TRACE
+#define TRACE_LOCALS() unsigned long long _trv[TRACE_SLOTS] = {0}
 #define TRACE_T0() const long long _tr0 = clock64()
-#define TRACE_ADD(p, slot) \
-  do { if ((p).trace) atomicAdd((p).trace + (size_t)blockIdx.x * TRACE_SLOTS + (slot), (unsigned long long)(clock64() - _tr0)); } while (0)
+#define TRACE_ADD(p, slot) (_trv[(slot)] += (unsigned long long)(clock64() - _tr0))
+#define TRACE_FLUSH(p)                                                                       \
+  do {                                                                                       \
+    if ((p).trace)                                                                           \
+      for (int _i = 2; _i < TRACE_SLOTS; ++_i)                                               \
+        if (_trv[_i]) atomicAdd((p).trace + (size_t)blockIdx.x * TRACE_SLOTS + _i, _trv[_i]); \
+  } while (0)
 #define TRACE_SET(p, slot, v) \
   do { if ((p).trace) (p).trace[(size_t)blockIdx.x * TRACE_SLOTS + (slot)] = (unsigned long long)(v); } while (0)
 #else
+#define TRACE_LOCALS() do {} while (0)
 #define TRACE_T0() do {} while (0)
 #define TRACE_ADD(p, slot) do {} while (0)
+#define TRACE_FLUSH(p) do {} while (0)
 #define TRACE_SET(p, slot, v) do {} while (0)
 #endif
 

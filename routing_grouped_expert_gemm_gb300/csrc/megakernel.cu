@@ -51,8 +51,8 @@ __device__ __forceinline__ int sf_offset(int r, int kb) { return (r & 31) * 16 +
 // ------------------------------------------------------------------ gather (dispatch)
 // Ring slot m % slots receives schedule rows [m b, min((m+1) b, R)) of x, at
 // ring row (row - m b).  Gather CTA g takes the minibatch's M-tiles g, g + G,
-// ...; its warps take the tile's rows.  MXFP8: each row is quantised on the
-// way (E4M3 codes into the ring, E8M0 scales into the tile's scale blocks).
+// ...; its warps take the tile's rows.  MXFP8: the per-token E4M3 codes go to
+// the ring and their E8M0 scales into the tile's scale blocks.
 __device__ void gather_copy_row(const FwdParams& p, const bf16* src_row, bf16* dst_row) {
   const int lane = threadIdx.x & 31;
   const int nv = p.D / 8;  // 16-byte vectors per row
@@ -75,37 +75,36 @@ __device__ void gather_copy_row(const FwdParams& p, const bf16* src_row, bf16* d
   }
 }
 
-__device__ void gather_quantize_row(const FwdParams& p, const bf16* src_row, uint8_t* dst_row, uint8_t* sf_tile,
-                                    int r_in_tile) {
+// MXFP8: x was quantised once per token before this kernel (codes xq [T, D],
+// scales xs [T, D/32]); the gather copies a token's codes into the ring and
+// its scale words (one per 128-wide K step) into the tile's scale blocks.
+__device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, uint8_t* sf_tile, int r_in_tile) {
   const int lane = threadIdx.x & 31;
-  const int nblk = p.D / 32;  // lane l takes 32-element blocks l, l + 32, ...
-#pragma unroll 2
-  for (int blk = lane; blk < nblk + (32 - nblk % 32) % 32; blk += 32) {
-    const bool on = blk < nblk;
-    float v[32];
-    if (on) {
-      load_bf16x32(src_row + blk * 32, v);
-    } else {
+  const int nv = p.D / 16;  // 16-byte vectors of codes
+  constexpr int UNR = 16;   // D <= 8192 in one pass
+  const uint4* src = reinterpret_cast<const uint4*>(p.xq + (size_t)t * p.D);
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+  for (int base = 0; base < nv; base += 32 * UNR) {
+    uint4 v[UNR];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) v[u] = __ldg(src + i);
     }
-    uint32_t q[8];
-    const uint32_t code = mx_quantize32(v, q);
-    if (on) {
-      uint4* dst = reinterpret_cast<uint4*>(dst_row + blk * 32);
-      dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) dst[i] = v[u];
     }
-    // four consecutive lanes hold the four K-blocks of one 128-wide K step
-    uint32_t word = code << (8 * (blk & 3));
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (on && (blk & 3) == 0)
-      *reinterpret_cast<uint32_t*>(sf_tile + (size_t)(blk >> 2) * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = word;
   }
+  const int nkg = p.D / BK_MX;
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.xs + (size_t)t * (p.D / 32));
+  for (int kg = lane; kg < nkg; kg += 32)
+    *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = __ldg(sw + kg);
 }
 
 __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
+  TRACE_LOCALS();
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int m = 0; m < p.n_mb; ++m) {
@@ -117,7 +116,7 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
         TRACE_ADD(p, TR_GATHER_WAIT);
       }
       __syncthreads();
-      if (*s_flag == 0) return;
+      if (*s_flag == 0) break;
     }
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
@@ -130,8 +129,8 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
         for (int r = warp; r < rows; r += nwarps) {
           const int t = p.sched[(size_t)(p0 + r) * 3];
           const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
-          gather_quantize_row(p, p.x + (size_t)t * p.D, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
-                              p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
+          gather_copy_row_mx(p, t, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
+                             p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
         }
       }
     } else {  // contiguous row ranges per CTA, rows strided over its warps
@@ -150,6 +149,7 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
       red_release_add_gpu(p.counters + ctr_filled(p, m), 1);
     }
   }
+  TRACE_FLUSH(p);
 }
 
 // ------------------------------------------------------------------ operand selection
@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
       // arrives; with direct dispatch every lane also gathers 4 of the tile's
       // 128 token rows per K step, and for MXFP8 writes their scale words)
       const bool leader = lane == 0;
+      TRACE_LOCALS();
       if (leader) {
         prefetch_tensormap(&maps.x);
         prefetch_tensormap(&maps.ring_x);
@@ -613,6 +614,15 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
               for (int i = gather_a ? 1 : 0; i < 3; ++i)
                 bulk_load(ssf + i * SF_BLOCK_BYTES, src[i], SF_BLOCK_BYTES, &full[stage]);
             }
+            // L2 prefetch of the tiles p.l2_prefetch K steps ahead: the loads that
+            // follow then wait for L2, not for HBM
+            const int kp = kb + p.l2_prefetch;
+            if (p.l2_prefetch > 0 && kp < o.nk) {
+              const int kcp = kp * (mx ? BK_MX : BK);
+              if (!gather_a) tma_prefetch_2d(o.a, kcp, t.a_row);
+              tma_prefetch_2d(o.b0, kcp, o.b_row);
+              if (o.b1) tma_prefetch_2d(o.b1, kcp, o.b_row);
+            }
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -622,10 +632,12 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
       if (leader)
         for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
           mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, p.status, p.timeout_ns);
+      if (leader) TRACE_FLUSH(p);
       __syncwarp();
     } else if (warp == 1) {
       // ---------------- MMA issuer
       if (elect_one()) {
+        TRACE_LOCALS();
         const uint32_t idesc = idesc_bf16_f32(BM, 256);
         const uint32_t idesc_mx = idesc_mxf8_e4m3(BM, 256);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -676,6 +688,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         }
         mma_commit(drain);
         mbar_wait(drain, 0, p.status, p.timeout_ns);
+        TRACE_FLUSH(p);
       }
       __syncwarp();
     } else if (warp >= 2 && warp < 6) {
@@ -684,6 +697,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
       const int row = q * 32 + lane;
       uint32_t acc = 0, acc_phase = 0;
       bool routed_done = false;
+      TRACE_LOCALS();
       for (int ti = cta; ti < n_tasks; ti += p.n_gemm) {
         const Task t = p.tasks[ti];
         // one thread waits and decides for all four warps, so that they agree
@@ -732,6 +746,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         }
         if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
       }
+      if (threadIdx.x == 64) TRACE_FLUSH(p);
     }
     tc_fence_before();
     __syncthreads();
@@ -744,9 +759,11 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   // ---------------- combine without a shared expert: every CTA, once all routed rows are stored
   if (!has_shared) {
     if (threadIdx.x == 0) {
+      TRACE_LOCALS();
       TRACE_T0();
       *s_flag = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
       TRACE_ADD(p, TR_FINAL_WAIT);
+      TRACE_FLUSH(p);
     }
     __syncthreads();
     if (*s_flag) combine_role(p);
