@@ -145,6 +145,24 @@ def dist_setup(n_gpus):
     return world, rank, local
 
 
+def reduce_max(v: float, world: int) -> float:
+    """Max of v over all ranks (the slowest replica sets the time).  Works with
+    the nccl (GPU tensor) and gloo (CPU tensor) backends."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job tokens/s of `world` independent replicas timed together."""
+    return world * tokens_per_step * steps / (elapsed_ms / 1000.0)
+
+
 # ----------------------------------------------------------------------------- oracle timing
 def time_oracle(inp, seconds: float):
     """Oracle on a contiguous token slice sized for about `seconds` of CPU time."""
@@ -337,12 +355,7 @@ def run_ours(args, world, rank, local):
     rgbuild.build()
 
     def allmax(v):
-        if world == 1:
-            return v
-        import torch.distributed as dist
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world)
 
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -364,7 +377,7 @@ def run_ours(args, world, rank, local):
     achieved = flops / (mega_mean / 1000.0) / 1e12
     line = {
         "metric": METRIC,
-        "value": world * T * args.steps / (elapsed_ms / 1000.0), "unit": "tokens/s", "n_gpus": world,
+        "value": replica_throughput(world, T, args.steps, elapsed_ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.precision == "bf16" else "mxfp8 (e4m3 + e8m0) routed, bf16 shared",
@@ -386,7 +399,7 @@ def run_ours(args, world, rank, local):
     }
     line["tflops_frac_of_peak"] = line["tflops"] / (world * peak)
     if e2e:
-        line["e2e"] = {"value": world * T * args.steps / (e2e["ms"] / 1000.0), "unit": "tokens/s",
+        line["e2e"] = {"value": replica_throughput(world, T, args.steps, e2e["ms"]), "unit": "tokens/s",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
     cpu = None
     if world == 1 and not args.no_cpu_baseline and rank == 0:
@@ -407,7 +420,7 @@ def run_ours(args, world, rank, local):
         m_ach = mshape.flops() / (m_mega / 1000.0) / 1e12
         line["mxfp8"] = {
             "workload": "dsv3_mxfp8: DSV3 shape, uniform routing, routed experts MXFP8, shared expert BF16",
-            "value": world * mshape.T * args.steps / (m_el / 1000.0), "unit": "tokens/s",
+            "value": replica_throughput(world, mshape.T, args.steps, m_el), "unit": "tokens/s",
             "ms_per_step": m_el / args.steps, "tflops": world * mshape.flops() * args.steps / (m_el / 1000.0) / 1e12,
             "gather_ctas": args.gather_ctas_mx,
             "phases_ms_mean": {"router_topk": statistics.mean(mres["router_ms"]),
