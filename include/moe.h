@@ -89,6 +89,13 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe
  *   timeout_ms limit of every device-side wait (0 = 2000 ms)
  *   l2_prefetch  K steps ahead that the GEMM producers prefetch operand tiles
  *              into L2 (0 = off, the default: on DSV3 it measured slower)
+ *   mma_pair   1: the GEMM CTAs run as pairs (clusters of 2) and each expert
+ *              tile is one tcgen05.mma.cta_group::2 of 256 rows, the pair's
+ *              two 128-row M-tiles sharing the weight tile, each CTA loading
+ *              half of it (half the operand bytes per SM of the one-CTA tile);
+ *              a segment with an odd number of M-tiles pads its last pair.
+ *              bf16 precision with ring dispatch only (MOE_ERR_INVALID_ARG
+ *              otherwise); gather_ctas must be even.  0: one CTA per tile.
  * Zero for minibatch / ring_slots / gather_ctas / lag picks the defaults
  * (8192 / 4 / 8 / 1).
  */
@@ -109,7 +116,8 @@ typedef struct moe_config {
   int32_t timeout_ms;
   int32_t dispatch;
   int32_t l2_prefetch;
-  int32_t reserved[2];
+  int32_t mma_pair;
+  int32_t reserved[1];
 } moe_config;
 
 /*

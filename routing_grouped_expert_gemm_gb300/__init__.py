@@ -19,6 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300.so")
 if os.environ.get("MOE_TRACE_BUILD") == "1":  # profiling only: the MOE_TRACE variant of the same library
     LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300_trace.so")
+elif os.environ.get("MOE_DEBUG_BUILD") == "1":  # debugging only: the MOE_DEBUG_LOG variant
+    LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300_dbg.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 
 MOE_OK = 0
@@ -47,7 +49,7 @@ class moe_config(ctypes.Structure):
                 ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
                 ("gather_ctas", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32), ("lag", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("dispatch", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("mma_pair", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class moe_weights(ctypes.Structure):
@@ -95,6 +97,8 @@ def lib():
     L.moe_route_static_scratch_bytes.restype = sz
     L.moe_testing_mx_tile.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_mx_tile.restype = ctypes.c_int
+    L.moe_testing_pair_tile.argtypes = [vp, vp, vp, vp, vp]
+    L.moe_testing_pair_tile.restype = ctypes.c_int
     L.moe_error_string.argtypes = [ctypes.c_int]
     L.moe_error_string.restype = ctypes.c_char_p
     _lib = L
@@ -144,7 +148,7 @@ class Plan:
 
 def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
                     ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0, dispatch=MOE_DISPATCH_RING,
-                    l2_prefetch=0) -> Plan:
+                    l2_prefetch=0, mma_pair=0) -> Plan:
     if isinstance(score_fn, str):
         score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
     if isinstance(precision, str):
@@ -152,7 +156,7 @@ def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precis
     if isinstance(dispatch, str):
         dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
-                     lag, timeout_ms, dispatch, l2_prefetch)
+                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair)
     h = ctypes.c_void_p()
     rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
     if rc != MOE_OK:

@@ -20,7 +20,9 @@ OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
 TRACE_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_trace.so")
-SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu", "probe_mx.cu"]
+DEBUG_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_dbg.so")
+SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu", "probe_mx.cu",
+           "probe_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -54,16 +56,19 @@ def _stale(lib_path: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False,
+          debug_log: bool = False) -> str:
     """Build the library; trace=True builds the MOE_TRACE variant (per-CTA wait
-    timers in the persistent kernel) as _lib/libmoe_gb300_trace.so instead."""
-    lib_path = TRACE_LIB_PATH if trace else LIB_PATH
-    obj_dir = OBJ + ("_trace" if trace else "")
+    timers in the persistent kernel) as _lib/libmoe_gb300_trace.so instead;
+    debug_log=True the MOE_DEBUG_LOG variant (per-CTA progress records and
+    bounds checks written to host memory) as _lib/libmoe_gb300_dbg.so."""
+    lib_path = TRACE_LIB_PATH if trace else (DEBUG_LIB_PATH if debug_log else LIB_PATH)
+    obj_dir = OBJ + ("_trace" if trace else ("_dbg" if debug_log else ""))
     if not force and not _stale(lib_path):
         return lib_path
     os.makedirs(obj_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
-    defines = ("MOE_TRACE",) if trace else ()
+    defines = ("MOE_TRACE",) if trace else (("MOE_DEBUG_LOG",) if debug_log else ())
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, ptxas_v, defines, obj_dir), SOURCES))
     tmp = lib_path + ".tmp"
@@ -76,4 +81,5 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, tra
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_v="-v" in sys.argv, trace="--trace" in sys.argv,
+                debug_log="--debug-log" in sys.argv))

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -15,6 +16,7 @@ cudaError_t launch_router(const RouterMaps& maps, const FwdParams& p, cudaStream
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream);
 int megakernel_smem_bytes();
+int megakernel_pair_max_ctas();
 cudaError_t launch_mx_quantize(const bf16* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st);
 size_t mx_scale_bytes(int64_t rows, int64_t K);
@@ -43,8 +45,10 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.max_segs = L.n_mb + c.E;
   L.n_mtiles_max = ceil_div(L.R, BM) + L.n_mb + c.E;
   L.n_smtiles = c.I_s > 0 ? L.n_chunks : 0;
-  L.n_tasks_max = L.n_mtiles_max * (c.I / BN_UP + c.D / BN_DOWN) +
-                  (c.I_s > 0 ? L.n_smtiles * (c.I_s / BN_UP + c.D / BN_DOWN) : 0);
+  // CTA pairs pad every expert segment and the shared token tiles to an even count
+  const int64_t pad_seg = c.mma_pair ? L.max_segs : 0, pad_sh = c.mma_pair ? 1 : 0;
+  L.n_tasks_max = (L.n_mtiles_max + pad_seg) * (c.I / BN_UP + c.D / BN_DOWN) +
+                  (c.I_s > 0 ? (L.n_smtiles + pad_sh) * (c.I_s / BN_UP + c.D / BN_DOWN) : 0);
   L.n_counters = 1 + 3 * L.n_mb + L.n_mtiles_max + L.n_smtiles;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -76,7 +80,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.xs = take(mx ? (size_t)T * (c.D / 32) : 0);
   L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
-  L.Y = take((size_t)L.R * c.D * 2);
+  L.Y = take((size_t)L.n_chunks * BM * c.k * c.D * 2);  // blocked by token tile, see FwdParams::Y
 #ifdef MOE_TRACE
   L.trace = take(sizeof(unsigned long long) * TRACE_SLOTS * 1024);
 #endif
@@ -150,6 +154,10 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.minibatch < BM || c.minibatch > 32768 || c.minibatch % BM) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.ring_slots < c.lag + 1 || c.ring_slots > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((c.T_max * c.k + c.minibatch - 1) / c.minibatch > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;  // schedule smem
+  if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
+  if (c.mma_pair && (c.precision != MOE_PREC_BF16 || c.dispatch != MOE_DISPATCH_RING || (c.gather_ctas & 1) ||
+                     (c.gemm_ctas & 1)))
+    return MOE_ERR_INVALID_ARG;
   if (c.dispatch == MOE_DISPATCH_DIRECT) c.gather_ctas = 0;  // the GEMM producers gather
   if ((c.dispatch == MOE_DISPATCH_RING && c.gather_ctas < 1) || c.gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
 
@@ -158,8 +166,12 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED_DEVICE;
-  const int gemm = c.gemm_ctas > 0 ? c.gemm_ctas : prop.multiProcessorCount - c.gather_ctas;
-  if (gemm < 1 || c.gather_ctas + gemm > prop.multiProcessorCount) return MOE_ERR_INVALID_ARG;
+  // CTAs resident at once: one per SM, or for CTA pairs as many as whole
+  // clusters of 2 can be placed
+  const int resident = c.mma_pair ? megakernel_pair_max_ctas() : prop.multiProcessorCount;
+  if (resident < 2) return MOE_ERR_CUDA;
+  const int gemm = c.gemm_ctas > 0 ? c.gemm_ctas : resident - c.gather_ctas;
+  if (gemm < (c.mma_pair ? 2 : 1) || c.gather_ctas + gemm > resident) return MOE_ERR_INVALID_ARG;
 
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -250,6 +262,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.score_fn = c.score_fn;
   p.mx = mx ? 1 : 0;
   p.direct = c.dispatch == MOE_DISPATCH_DIRECT ? 1 : 0;
+  p.pair = c.mma_pair;
   p.b = c.minibatch;
   p.slots = c.ring_slots;
   p.G = c.gather_ctas;
@@ -301,6 +314,11 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   cudaMemsetAsync(p.trace, 0, sizeof(unsigned long long) * TRACE_SLOTS * 1024, stream);
 #endif
 
+#ifdef MOE_DEBUG_LOG
+  // debugging builds only: the address of mapped pinned host memory for the
+  // progress records, [grid, DBG_SLOTS] int32, given by the environment
+  if (const char* dbg = std::getenv("MOE_DEBUG_LOG_PTR")) p.dbg = reinterpret_cast<int*>(std::strtoull(dbg, nullptr, 0));
+#endif
   // tensor maps (raw pointers are baked in, so they are encoded per call)
   RouterMaps rm;
   TensorMaps tm;
@@ -308,6 +326,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   std::memset(&tm, 0, sizeof(tm));
   const int64_t ring_rows = (int64_t)c.ring_slots * c.minibatch;
   const uint32_t wr_box = (uint32_t)(p.n_router_cols > 256 ? p.n_router_cols / 2 : p.n_router_cols);
+  const uint32_t down_box = c.mma_pair ? 128u : (uint32_t)BN_DOWN;  // pairs: each CTA loads half the columns
   int rc = MOE_OK;
   rc |= encode_bf16_2d(pl, &rm.x, x, T, c.D, BM);
   rc |= encode_bf16_2d(pl, &rm.wr, w->W_router, c.E, c.D, wr_box);
@@ -329,13 +348,13 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
     rc |= encode_bf16_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
-    rc |= encode_bf16_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, BN_DOWN);
+    rc |= encode_bf16_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, down_box);
   }
   if (shared) {
     rc |= encode_bf16_2d(pl, &tm.ws_up, w->Ws_up, c.I_s, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.ws_gate, w->Ws_gate, c.I_s, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.h_s, p.h_s, T, c.I_s, BM);
-    rc |= encode_bf16_2d(pl, &tm.ws_down, w->Ws_down, c.D, c.I_s, BN_DOWN);
+    rc |= encode_bf16_2d(pl, &tm.ws_down, w->Ws_down, c.D, c.I_s, down_box);
   }
   if (rc != MOE_OK) return MOE_ERR_INVALID_ARG;
 

@@ -32,6 +32,11 @@ constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK_BYTES;
 constexpr int MX_STAGE_TX = STAGE_BYTES + SF_STAGE_BYTES;
 constexpr int STAGE_STRIDE = 51200;               // 1024-aligned stage pitch (BF16 and MXFP8)
 static_assert(STAGE_BYTES + SF_STAGE_BYTES <= STAGE_STRIDE && STAGE_STRIDE % 1024 == 0, "stage pitch");
+// CTA pairs (cta_group::2): each CTA stages its 128 A rows and half of the
+// 256 B rows (up or gate for GEMM1, one half of the output columns for GEMM2)
+constexpr int PAIR_B_STAGE_BYTES = 128 * BK * 2;  // 16 KB
+constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + PAIR_B_STAGE_BYTES;  // 32 KB per CTA
+constexpr int PAIR_STAGES = 6;
 constexpr int SF_TMEM_COL = 256;                  // MXFP8: scale columns after the single accumulator
 constexpr int ACC_COLS = 256;    // fp32 accumulator columns per tile
 constexpr int MEGA_THREADS = 256;  // 8 warps
@@ -72,6 +77,7 @@ struct FwdParams {
   int score_fn;
   int mx;               // routed experts in MXFP8 (1) or BF16 (0)
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
+  int pair;             // 1: GEMM CTAs run as pairs, tasks 2i and 2i + 1 share one cta_group::2 MMA
   int b, slots, G, n_gemm, lag;
   int n_mb, R;          // minibatches, routes (T*k)
   int N1, N2, N1s, N2s; // column tiles: I/128, D/256, I_s/128, D/256
@@ -108,9 +114,12 @@ struct FwdParams {
   const uint8_t* w_gate_sf;
   const uint8_t* w_down_sf;
   bf16* h_s;          // [T, I_s]
-  __half* Y;          // [R, D] fp16, token order (row j = t*k + slot)
+  __half* Y;          // fp16 staging rows of the routed outputs, blocked: for token tile tt = t / 128 and
+                      // column tile n (256 columns), block (tt, n) holds [128 tokens][k slots][256 columns]
+                      // contiguously, so one shared-expert down tile's combine reads one 128 k 512-byte block
   bf16* out;          // [T, D]
   unsigned long long* trace;  // [grid, TRACE_SLOTS] when built with MOE_TRACE, else null
+  int* dbg;           // MOE_DEBUG_LOG builds: [grid, DBG_SLOTS] progress records in host memory, else null
 };
 
 // Optional per-CTA timing of the persistent kernel (build with -DMOE_TRACE):
@@ -143,6 +152,43 @@ enum : int {
 #define TRACE_SET(p, slot, v) do {} while (0)
 #endif
 
+// Debug builds (-DMOE_DEBUG_LOG): each CTA records its progress and the first
+// failed bounds check in host memory (mapped pinned memory, readable by the
+// host even after the context is lost), one store + system fence per record.
+enum : int {
+  DBG_PHASE = 0, DBG_RANK, DBG_TMEM, DBG_PROD_UNIT, DBG_PROD_ISSUED, DBG_MMA_UNIT, DBG_MMA_STAGES, DBG_MMA_ACC,
+  DBG_EPI_UNIT, DBG_EPI_DONE, DBG_FAIL_SITE, DBG_FAIL_V0, DBG_FAIL_V1, DBG_FAIL_V2, DBG_PROD_WAIT, DBG_MMA_WAIT,
+  DBG_EPI_WAIT, DBG_EPI_TASK, DBG_SLOTS = 32
+};
+#ifdef MOE_DEBUG_LOG
+__device__ __forceinline__ void dbg_set(const FwdParams& p, int slot, int v) {
+  if (p.dbg) {
+    *reinterpret_cast<volatile int*>(p.dbg + (size_t)blockIdx.x * DBG_SLOTS + slot) = v;
+    __threadfence_system();
+  }
+}
+// false (and the first failure recorded) when cond does not hold: the caller skips the access
+__device__ __forceinline__ bool dbg_check(const FwdParams& p, bool cond, int site, int v0, int v1, int v2) {
+  if (cond) return true;
+  if (p.dbg) {
+    volatile int* d = p.dbg + (size_t)blockIdx.x * DBG_SLOTS;
+    if (d[DBG_FAIL_SITE] == 0) {
+      d[DBG_FAIL_V0] = v0;
+      d[DBG_FAIL_V1] = v1;
+      d[DBG_FAIL_V2] = v2;
+      d[DBG_FAIL_SITE] = site;
+      __threadfence_system();
+    }
+  }
+  return false;
+}
+#define DBG_SET(p, slot, v) dbg_set((p), (slot), (int)(v))
+#define DBG_CHECK(p, cond, site, v0, v1, v2) dbg_check((p), (cond), (site), (int)(v0), (int)(v1), (int)(v2))
+#else
+#define DBG_SET(p, slot, v) do {} while (0)
+#define DBG_CHECK(p, cond, site, v0, v1, v2) (true)
+#endif
+
 // counter indices
 __host__ __device__ inline int ctr_ydone() { return 0; }
 __host__ __device__ inline int ctr_filled(const FwdParams& p, int m) { return 1 + m; }
@@ -151,6 +197,10 @@ __host__ __device__ inline int ctr_r2(const FwdParams& p, int m) { return 1 + 2 
 __host__ __device__ inline int ctr_hready(const FwdParams& p, int mt) { return 1 + 3 * p.n_mb + mt; }
 __host__ __device__ inline int ctr_shready(const FwdParams& p, int mt) {
   return 1 + 3 * p.n_mb + p.n_mtiles_max + mt;
+}
+// the 256 staging columns of column tile n for route (token t, slot s)
+__host__ __device__ inline size_t y_offset(const FwdParams& p, int t, int s, int n) {
+  return ((((size_t)(t / BM) * p.N2 + n) * BM + (size_t)(t % BM)) * p.k + s) * BN_DOWN;
 }
 __host__ __device__ inline int n_counters(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
 
@@ -201,6 +251,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
   while (!mbar_try_wait(bar, parity)) {
+    if ((++it & 63u) == 0) {
+      if (ld_relaxed_gpu(status) != 0) return false;
+      if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) {
+        raise_status(status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// the same for a phase completed with the help of the other CTA of a pair
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status, long long timeout_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t it = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if ((++it & 63u) == 0) {
       if (ld_relaxed_gpu(status) != 0) return false;
       if (globaltimer_ns() - t0 > (uint64_t)timeout_ns) {

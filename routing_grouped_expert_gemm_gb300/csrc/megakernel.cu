@@ -41,7 +41,6 @@ __device__ __forceinline__ uint8_t* align_1024_mk(uint8_t* p) {
 
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
 constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
-constexpr int MEGA_SMEM_BYTES = STAGES * STAGE_STRIDE + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
 
 // ------------------------------------------------------------------ MXFP8 helpers
 // byte offset of (row r of a 128-row block, K-block kb of a 128-wide K step)
@@ -212,6 +211,24 @@ __device__ __forceinline__ void mx_scale_sources(const FwdParams& p, const Task&
 }
 
 // ------------------------------------------------------------------ epilogues
+// Handing an accumulator buffer back to the MMA issuer after its last TMEM
+// read: every epilogue thread arrives on the local barrier (one CTA per tile),
+// or one lane per warp arrives on the even CTA's barrier (CTA pairs).
+struct AccRelease {
+  uint64_t* local;
+  uint32_t remote;  // cluster address of the even CTA's barrier
+  bool pair;
+};
+__device__ __forceinline__ void release_acc(const AccRelease& r) {
+  tc_fence_before();
+  if (r.pair) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(r.remote);
+  } else {
+    mbar_arrive(r.local);
+  }
+}
+
 // 128 threads, thread r owns tile row r (TMEM lane r).
 __device__ __forceinline__ void store_row_bf16x32(bf16* dst, const float* v) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -268,7 +285,7 @@ __device__ __forceinline__ float4 load_f16x4(const __half* p) {
 
 // up/gate tile -> h = SiLU(gate) * up (bf16): TMEM columns [0,128) up, [128,256) gate.
 // dst: row 0 of the warp's rows, column 0 of the tile; ld: row stride (elements).
-__device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t ld, int nrows, uint64_t* tempty) {
+__device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t ld, int nrows, const AccRelease& rel) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < BN_UP; c += 32) {
@@ -277,8 +294,7 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
     tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + c), g);
     tmem_ld_wait();
     if (c + 32 == BN_UP) {  // last TMEM read of this tile: hand the accumulator back
-      tc_fence_before();
-      mbar_arrive(tempty);
+      release_acc(rel);
     }
     float h[32];
 #pragma unroll
@@ -298,7 +314,7 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
 // tile's scale block (this tile's 128 columns are one 128-wide K step of the
 // down projection).  The accumulator is handed back after the last TMEM read.
 __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf_block, int row, bool valid,
-                                   uint64_t* tempty) {
+                                   const AccRelease& rel) {
   uint32_t q[4][8];
   uint32_t scales = 0;
 #pragma unroll
@@ -308,8 +324,7 @@ __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf
     tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + 32 * c), g);
     tmem_ld_wait();
     if (c == 3) {
-      tc_fence_before();
-      mbar_arrive(tempty);
+      release_acc(rel);
     }
     float h[32];
 #pragma unroll
@@ -327,9 +342,10 @@ __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf
   }
 }
 
-// routed down-projection tile -> fp16 staging rows Y[j] (j from the schedule table)
-__device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, size_t D, int col0, int j_mine, int nrows,
-                                  uint64_t* tempty) {
+// routed down-projection tile -> fp16 staging rows (route j = t k + slot from
+// the schedule table); y_mine: offset of this thread's row's 256-column segment
+__device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, long long y_mine, int nrows,
+                                  const AccRelease& rel) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < BN_DOWN; c += 32) {
@@ -337,8 +353,7 @@ __device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, size_
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
     if (c + 32 == BN_DOWN) {
-      tc_fence_before();
-      mbar_arrive(tempty);
+      release_acc(rel);
     }
     float v[32];
 #pragma unroll
@@ -347,11 +362,10 @@ __device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, size_
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
-      const int jr = __shfl_sync(0xffffffffu, j_mine, rr);
+      const long long yr = __shfl_sync(0xffffffffu, y_mine, rr);
       if (rr < nrows) {
         const float4 f = staged4(st, rr, cc);
-        *reinterpret_cast<uint2*>(Y + (size_t)jr * D + col0 + c + cc) = make_uint2(pack_f16x2_sat(f.x, f.y),
-                                                                                   pack_f16x2_sat(f.z, f.w));
+        *reinterpret_cast<uint2*>(Y + yr + c + cc) = make_uint2(pack_f16x2_sat(f.x, f.y), pack_f16x2_sat(f.z, f.w));
       }
     }
     __syncwarp();
@@ -364,13 +378,13 @@ __device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, size_
 // shared expert's down-projection epilogue and starts from its fp32 output;
 // without one, this pass runs once every routed output row is stored.
 __device__ __forceinline__ void accumulate_routed(const FwdParams& p, int t, int col, const float* g, float* acc) {
-  const __half* y = p.Y + (size_t)t * p.k * p.D + col;
+  const __half* y = p.Y + y_offset(p, t, 0, col / BN_DOWN) + col % BN_DOWN;
 #pragma unroll
   for (int s = 0; s < TOPK_MAX; ++s) {
     if (s < p.k) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 f = load_f16x4(y + (size_t)s * p.D + 4 * i);
+        const float4 f = load_f16x4(y + (size_t)s * BN_DOWN + 4 * i);
         acc[4 * i + 0] = fmaf(g[s], f.x, acc[4 * i + 0]);
         acc[4 * i + 1] = fmaf(g[s], f.y, acc[4 * i + 1]);
         acc[4 * i + 2] = fmaf(g[s], f.z, acc[4 * i + 2]);
@@ -386,57 +400,102 @@ __device__ __forceinline__ void load_g(const FwdParams& p, int t, bool valid, fl
 }
 
 // shared-expert down projection + combine: out = bf16(y_s + sum_slot g * Y[t k + slot]),
-// y_s in fp32 straight from TMEM; t0 = token of the warp's first row
+// y_s in fp32 straight from TMEM; t0 = token of the warp's first row.
+// The staging rows are the combine's only large read (k D fp16 per token):
+// lane l handles rows 8i + l/4 and 8 columns (16 bytes) at 8 (l % 4) of each
+// 32-column chunk, and a chunk's 4 rows x 8 slots of loads are all issued
+// before the first is used, so that enough bytes are in flight to cover
+// the memory latency (the tile was prefetched into L2 by the producer).
+constexpr int CMB_SLOTS = 8;  // slots per batch of loads
+
+__device__ __forceinline__ void fma_f16x8(float* acc, float g, uint4 w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+    acc[2 * i] = fmaf(g, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(g, f.y, acc[2 * i + 1]);
+  }
+}
+
 __device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdParams& p, int t0, int col0,
-                                        int nrows, uint64_t* tempty) {
+                                        int nrows, const AccRelease& rel) {
   const int lane = threadIdx.x & 31;
   const int k = p.k;
 #pragma unroll
   for (int s = 0; s < TOPK_MAX; ++s) st.g[lane][s] = (lane < nrows && s < k) ? p.topk_w[(size_t)(t0 + lane) * k + s] : 0.0f;
-  // the k staging rows of a token are read once: ask L2 for them two chunks
-  // ahead (lane = row; one 128-byte line per slot and chunk)
-  const __half* yrow = p.Y + (size_t)(t0 + lane) * k * p.D + col0;
-  auto prefetch_chunk = [&](int c) {
-    if (lane < nrows && c < BN_DOWN)
-      for (int s = 0; s < k; ++s) prefetch_l2(yrow + (size_t)s * p.D + c);
-  };
-  prefetch_chunk(0);
-  prefetch_chunk(32);
-#pragma unroll 1
-  for (int c = 0; c < BN_DOWN; c += 32) {
-    prefetch_chunk(c + 64);
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
-    tmem_ld_wait();
-    if (c + 32 == BN_DOWN) {
-      tc_fence_before();
-      mbar_arrive(tempty);
+  const int cc = 8 * (lane & 3);
+  __syncwarp();  // g visible to the warp
+  // rows 8i + lane/4 of a half h: i = 2h, 2h + 1
+  auto load_half = [&](uint4 (&yv)[2][CMB_SLOTS], int c, int h, int s0) {
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int rr = 8 * (2 * h + ii) + (lane >> 2);
+      const __half* y = p.Y + y_offset(p, t0 + rr, s0, col0 / BN_DOWN) + c + cc;
+#pragma unroll
+      for (int s = 0; s < CMB_SLOTS; ++s)
+        yv[ii][s] = (rr < nrows && s0 + s < k) ? *reinterpret_cast<const uint4*>(y + (size_t)s * BN_DOWN)
+                                               : make_uint4(0u, 0u, 0u, 0u);
     }
-    float v[32];
+  };
+  auto fma_half = [&](float (&acc)[2][8], const uint4 (&yv)[2][CMB_SLOTS], int h, int s0) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-    stage_block(st, v);
-#pragma unroll 2
-    for (int i = 0; i < 8; ++i) {
-      const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
+    for (int ii = 0; ii < 2; ++ii) {
+      const int rr = 8 * (2 * h + ii) + (lane >> 2);
+#pragma unroll
+      for (int s = 0; s < CMB_SLOTS; ++s)
+        if (s0 + s < k) fma_f16x8(acc[ii], st.g[rr][s0 + s], yv[ii][s]);
+    }
+  };
+  auto finish_half = [&](const uint4 (&yv0)[2][CMB_SLOTS], int c, int h) {
+    float acc[2][8];
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int rr = 8 * (2 * h + ii) + (lane >> 2);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[ii][j] = st.v[rr][cc + j];  // the shared expert's fp32 output
+    }
+    fma_half(acc, yv0, h, 0);
+#pragma unroll 1
+    for (int s0 = CMB_SLOTS; s0 < k; s0 += CMB_SLOTS) {  // k > 8: further slot batches
+      uint4 yv[2][CMB_SLOTS];
+      load_half(yv, c, h, s0);
+      fma_half(acc, yv, h, s0);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int rr = 8 * (2 * h + ii) + (lane >> 2);
       if (rr < nrows) {
-        const int t = t0 + rr;
-        float4 acc = staged4(st, rr, cc);
-        const __half* y = p.Y + (size_t)t * k * p.D + col0 + c + cc;
-#pragma unroll
-        for (int s = 0; s < TOPK_MAX; ++s) {
-          if (s < k) {
-            const float gs = st.g[rr][s];
-            const float4 f = load_f16x4(y + (size_t)s * p.D);
-            acc.x = fmaf(gs, f.x, acc.x);
-            acc.y = fmaf(gs, f.y, acc.y);
-            acc.z = fmaf(gs, f.z, acc.z);
-            acc.w = fmaf(gs, f.w, acc.w);
-          }
-        }
-        *reinterpret_cast<uint2*>(p.out + (size_t)t * p.D + col0 + c + cc) = pack_bf16x4(acc);
+        uint4 o;
+        o.x = pack_bf16x2(acc[ii][0], acc[ii][1]);
+        o.y = pack_bf16x2(acc[ii][2], acc[ii][3]);
+        o.z = pack_bf16x2(acc[ii][4], acc[ii][5]);
+        o.w = pack_bf16x2(acc[ii][6], acc[ii][7]);
+        *reinterpret_cast<uint4*>(p.out + (size_t)(t0 + rr) * p.D + col0 + c + cc) = o;
       }
     }
+  };
+#pragma unroll 1
+  for (int c = 0; c < BN_DOWN; c += 32) {
+    // staging-row loads of the first half go out before the TMEM read and
+    // those of the second half before the first half is summed, so that the
+    // latencies overlap
+    uint4 ya[2][CMB_SLOTS], yb[2][CMB_SLOTS];
+    load_half(ya, c, 0, 0);
+    {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+      tmem_ld_wait();
+      if (c + 32 == BN_DOWN) {
+        release_acc(rel);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) st.v[lane][j] = __uint_as_float(r[j]);
+      __syncwarp();
+    }
+    load_half(yb, c, 1, 0);
+    finish_half(ya, c, 0);
+    finish_half(yb, c, 1);
     __syncwarp();
   }
 }
@@ -458,26 +517,60 @@ __device__ void combine_role(const FwdParams& p) {
 }
 
 // ------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(MEGA_THREADS, 1)
-    moe_megakernel(const __grid_constant__ TensorMaps maps, const FwdParams p) {
+// Stage geometry of the two kernel flavours: one CTA per tile (A 128 rows + B
+// 256 rows per stage, MXFP8 scale blocks after them) or CTA pairs (A 128 rows
+// + B 128 rows per CTA and stage).
+template <bool kPair>
+struct MegaGeom {
+  static constexpr int stages = kPair ? PAIR_STAGES : STAGES;
+  static constexpr int stride = kPair ? PAIR_STAGE_BYTES : STAGE_STRIDE;
+  static constexpr int smem_bytes = stages * stride + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+};
+static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448, "shared memory");
+
+template <bool kPair>
+__device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
+  if constexpr (kPair) {
+    tmem_alloc_pair<TMEM_COLS>(slot);
+    tmem_relinquish_pair();
+  } else {
+    tmem_alloc<TMEM_COLS>(slot);
+    tmem_relinquish();
+  }
+}
+
+// Task walk: a GEMM CTA takes units first, first + step, ...; a unit is one
+// task, or with CTA pairs two consecutive tasks (2u: even CTA, 2u + 1: odd CTA)
+// that share one weight tile.
+struct TaskWalk {
+  int first, step, n_units, rank;
+  bool pair;
+  __device__ __forceinline__ int task(int u) const { return pair ? 2 * u + rank : u; }
+};
+
+template <bool kPair>
+__device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParams& p) {
+  using G = MegaGeom<kPair>;
+  constexpr int NST = G::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024_mk(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_STRIDE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * G::stride);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* empty = bars + NST;
+  uint64_t* tfull = bars + 2 * NST;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = s_flag + 1;
-  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + STAGES * STAGE_STRIDE + 256);
+  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + NST * G::stride + 256);
   // MXFP8 needs TMEM columns for the scales: one accumulator buffer instead of two
   const uint32_t n_acc = p.mx ? 1u : 2u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
   if (threadIdx.x == 0) TRACE_SET(p, TR_START_NS, globaltimer_ns());
+  if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 1);
   const bool has_shared = p.N1s > 0;
 
   if (is_gather) {
@@ -486,34 +579,49 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   } else {
     const int cta = blockIdx.x - p.G;
     const int n_tasks = p.meta[META_N_TASKS];
+    TaskWalk walk;
+    walk.pair = kPair;
+    walk.rank = kPair ? (int)(cluster_ctarank() & 1u) : 0;
+    walk.first = kPair ? cta >> 1 : cta;
+    walk.step = kPair ? p.n_gemm >> 1 : p.n_gemm;
+    walk.n_units = kPair ? n_tasks >> 1 : n_tasks;
+    const bool leader = walk.rank == 0;  // the CTA that issues the MMAs
     if (threadIdx.x == 0) {
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < NST; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(&tfull[a], 1);
-        mbar_init(&tempty[a], 128);
+        mbar_init(&tempty[a], kPair ? 8 : 128);  // pairs: one arrival per epilogue warp of both CTAs
       }
       mbar_init(drain, 1);
       fence_barrier_init();
     }
-    if (warp == 1) {
-      tmem_alloc<TMEM_COLS>(tmem_slot);
-      tmem_relinquish();
-    }
+    if (warp == 1) tmem_alloc_all<kPair>(tmem_slot);
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // the other CTA's barriers exist before anything targets them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+      DBG_SET(p, DBG_RANK, walk.rank);
+      DBG_SET(p, DBG_TMEM, tmem);
+      DBG_SET(p, DBG_PHASE, 2);
+    }
+    // waits on barriers that the other CTA of a pair helps complete
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+      if constexpr (kPair) return mbar_wait_cluster(bar, parity, p.status, p.timeout_ns);
+      else return mbar_wait(bar, parity, p.status, p.timeout_ns);
+    };
 
     if (warp == 0) {
       // ---------------- TMA producer (whole warp: lane 0 waits, loads B and
       // arrives; with direct dispatch every lane also gathers 4 of the tile's
       // 128 token rows per K step, and for MXFP8 writes their scale words)
-      const bool leader = lane == 0;
+      const bool lead_lane = lane == 0;
       TRACE_LOCALS();
-      if (leader) {
+      if (lead_lane) {
         prefetch_tensormap(&maps.x);
         prefetch_tensormap(&maps.ring_x);
         prefetch_tensormap(&maps.w_up);
@@ -522,13 +630,18 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         prefetch_tensormap(&maps.w_down);
         if (p.direct) prefetch_tensormap(&maps.x_rows);
       }
+      // pairs: every load of both CTAs is counted on the even CTA's full barrier
+      const uint32_t full_even = kPair ? mapa_shared(full, 0) : 0u;
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
-        const Task t = p.tasks[ti];
+      for (int u = walk.first; u < walk.n_units && ok; u += walk.step) {
+        if (!DBG_CHECK(p, walk.task(u) < p.n_tasks_max, 1, u, walk.task(u), p.n_tasks_max)) break;
+        const Task t = p.tasks[walk.task(u)];
         int good = 1;
-        if (leader) {
+        if (lead_lane) {
+          DBG_SET(p, DBG_PROD_UNIT, u);
+          DBG_SET(p, DBG_PROD_WAIT, 2);
           TRACE_T0();
           if (t.dep0 >= 0 && !wait_counter_ge(p.counters + t.dep0, t.need0, p.status, p.timeout_ns)) good = 0;
           if (good && t.dep1 >= 0 && !wait_counter_ge(p.counters + t.dep1, t.need1, p.status, p.timeout_ns)) good = 0;
@@ -539,6 +652,10 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         const Operands o = task_operands(maps, p, t);
         const bool mx = task_is_mx(p, t.kind);
         const bool gather_a = p.direct && t.kind == TASK_R1;
+        // pairs: this CTA's half of B -- up (even) or gate (odd) rows for
+        // GEMM1, the first or second 128 output columns for GEMM2
+        const CUtensorMap* bmap_pair = o.b1 ? (walk.rank ? o.b1 : o.b0) : o.b0;
+        const int brow_pair = o.b1 ? o.b_row : o.b_row + 128 * walk.rank;
         // direct dispatch: lane l fetches tile rows 4l .. 4l+3 (rows past the
         // tile's end repeat its first token: discarded rows, in-bounds reads)
         int tok[4] = {0, 0, 0, 0};
@@ -560,134 +677,184 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         }
         for (int kb = 0; kb < o.nk; ++kb) {
           int free = 1;
-          if (leader) {
+          if (lead_lane) {
+            DBG_SET(p, DBG_PROD_WAIT, 1);
             TRACE_T0();
-            free = mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns) ? 1 : 0;
+            free = wait_bar(&empty[stage], phase ^ 1u) ? 1 : 0;
             TRACE_ADD(p, TR_PROD_EMPTY);
+            DBG_SET(p, DBG_PROD_WAIT, 0);
+            if (!DBG_CHECK(p, stage < (uint32_t)NST, 2, stage, phase, u)) free = 0;
           }
           if (!__shfl_sync(0xffffffffu, free, 0)) { ok = false; break; }
-          uint8_t* sa = smem + stage * STAGE_STRIDE;
+          uint8_t* sa = smem + stage * G::stride;
           uint8_t* sb = sa + A_STAGE_BYTES;
           uint8_t* ssf = sa + STAGE_BYTES;
           // a K step is 64 bf16 or 128 E4M3 elements: 128 bytes per row either way
           const int kc = kb * (mx ? BK_MX : BK);
-          if (gather_a) {
-            tma_gather4(sa + lane * 4 * 128, &maps.x_rows, &full[stage], kc, tok[0], tok[1], tok[2], tok[3]);
-            if (mx) {  // the tile's A scale block, written here rather than copied
-              const int d = kb & 3;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t w = 0;
-#pragma unroll
-                for (int dd = 0; dd < 4; ++dd)
-                  if (dd == d) w = sfw[dd][j];
-                *reinterpret_cast<uint32_t*>(ssf + sf_offset(4 * lane + j, 0)) = w;
-              }
-              if (kb + 4 < o.nk) {  // refill this slot with K step kb + 4
+          if constexpr (kPair) {
+            if (lead_lane) {
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)PAIR_STAGE_BYTES);
+              const uint32_t fb = full_even + stage * 8u;
+              tma_load_2d_pair(sa, o.a, fb, kc, t.a_row);
+              tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
+            }
+          } else {
+            if (gather_a) {
+              tma_gather4(sa + lane * 4 * 128, &maps.x_rows, &full[stage], kc, tok[0], tok[1], tok[2], tok[3]);
+              if (mx) {  // the tile's A scale block, written here rather than copied
+                const int d = kb & 3;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  const uint32_t w = *reinterpret_cast<const uint32_t*>(p.xs + (size_t)tok[j] * (nkg * 4) + (kb + 4) * 4);
+                  uint32_t w = 0;
 #pragma unroll
                   for (int dd = 0; dd < 4; ++dd)
-                    if (dd == d) sfw[dd][j] = w;
+                    if (dd == d) w = sfw[dd][j];
+                  *reinterpret_cast<uint32_t*>(ssf + sf_offset(4 * lane + j, 0)) = w;
                 }
+                if (kb + 4 < o.nk) {  // refill this slot with K step kb + 4
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint32_t w =
+                        *reinterpret_cast<const uint32_t*>(p.xs + (size_t)tok[j] * (nkg * 4) + (kb + 4) * 4);
+#pragma unroll
+                    for (int dd = 0; dd < 4; ++dd)
+                      if (dd == d) sfw[dd][j] = w;
+                  }
+                }
+                fence_proxy_async_smem();
               }
-              fence_proxy_async_smem();
             }
-          }
-          __syncwarp();
-          if (leader) {
-            // bytes the TMA engine delivers (the scale block written above is not counted)
-            const uint32_t tx = (mx ? (uint32_t)MX_STAGE_TX : (uint32_t)STAGE_BYTES) -
-                                (gather_a && mx ? (uint32_t)SF_BLOCK_BYTES : 0u);
-            mbar_arrive_expect_tx(&full[stage], tx);
-            if (!gather_a) tma_load_2d(sa, o.a, &full[stage], kc, t.a_row);
-            if (o.b1) {
-              tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
-              tma_load_2d(sb + B_STAGE_BYTES / 2, o.b1, &full[stage], kc, o.b_row);
-            } else {
-              tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
-            }
-            if (mx) {
-              const uint8_t* src[3];
-              mx_scale_sources(p, t, kb, src);
-              for (int i = gather_a ? 1 : 0; i < 3; ++i)
-                bulk_load(ssf + i * SF_BLOCK_BYTES, src[i], SF_BLOCK_BYTES, &full[stage]);
-            }
-            // L2 prefetch of the tiles p.l2_prefetch K steps ahead: the loads that
-            // follow then wait for L2, not for HBM
-            const int kp = kb + p.l2_prefetch;
-            if (p.l2_prefetch > 0 && kp < o.nk) {
-              const int kcp = kp * (mx ? BK_MX : BK);
-              if (!gather_a) tma_prefetch_2d(o.a, kcp, t.a_row);
-              tma_prefetch_2d(o.b0, kcp, o.b_row);
-              if (o.b1) tma_prefetch_2d(o.b1, kcp, o.b_row);
+            __syncwarp();
+            if (lead_lane) {
+              // bytes the TMA engine delivers (the scale block written above is not counted)
+              const uint32_t tx = (mx ? (uint32_t)MX_STAGE_TX : (uint32_t)STAGE_BYTES) -
+                                  (gather_a && mx ? (uint32_t)SF_BLOCK_BYTES : 0u);
+              mbar_arrive_expect_tx(&full[stage], tx);
+              if (!gather_a) tma_load_2d(sa, o.a, &full[stage], kc, t.a_row);
+              if (o.b1) {
+                tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
+                tma_load_2d(sb + B_STAGE_BYTES / 2, o.b1, &full[stage], kc, o.b_row);
+              } else {
+                tma_load_2d(sb, o.b0, &full[stage], kc, o.b_row);
+              }
+              if (mx) {
+                const uint8_t* src[3];
+                mx_scale_sources(p, t, kb, src);
+                for (int i = gather_a ? 1 : 0; i < 3; ++i)
+                  bulk_load(ssf + i * SF_BLOCK_BYTES, src[i], SF_BLOCK_BYTES, &full[stage]);
+              }
+              // L2 prefetch of the tiles p.l2_prefetch K steps ahead: the loads that
+              // follow then wait for L2, not for HBM
+              const int kp = kb + p.l2_prefetch;
+              if (p.l2_prefetch > 0 && kp < o.nk) {
+                const int kcp = kp * (mx ? BK_MX : BK);
+                if (!gather_a) tma_prefetch_2d(o.a, kcp, t.a_row);
+                tma_prefetch_2d(o.b0, kcp, o.b_row);
+                if (o.b1) tma_prefetch_2d(o.b1, kcp, o.b_row);
+              }
             }
           }
           ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (lead_lane) DBG_SET(p, DBG_PROD_ISSUED, issued);
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
       }
-      // the last STAGES loads this warp issued have landed before the CTA may exit
-      if (leader)
-        for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
-          mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, p.status, p.timeout_ns);
-      if (leader) TRACE_FLUSH(p);
+      // the last loads issued have landed before the CTA may leave (pairs: the
+      // even CTA's full barriers count both CTAs' loads, and the odd CTA waits
+      // for the even one at the cluster barrier below)
+      if (lead_lane && leader)
+        for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
+          wait_bar(&full[i % NST], (uint32_t)(i / NST) & 1u);
+      if (lead_lane) TRACE_FLUSH(p);
       __syncwarp();
     } else if (warp == 1) {
-      // ---------------- MMA issuer
-      if (elect_one()) {
+      // ---------------- MMA issuer (pairs: the even CTA issues for both)
+      if (leader && elect_one()) {
         TRACE_LOCALS();
-        const uint32_t idesc = idesc_bf16_f32(BM, 256);
+        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, 256);
         const uint32_t idesc_mx = idesc_mxf8_e4m3(BM, 256);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
-        for (int ti = cta; ti < n_tasks && ok; ti += p.n_gemm) {
-          const int kind = p.tasks[ti].kind;
+#ifdef MOE_DEBUG_LOG
+        int mma_stages = 0;
+#endif
+        for (int u = walk.first; u < walk.n_units && ok; u += walk.step) {
+          const int kind = p.tasks[walk.task(u)].kind;
           const bool mx = task_is_mx(p, kind);
           const int nk = task_nk(p, kind);
+          DBG_SET(p, DBG_MMA_UNIT, u);
+          DBG_SET(p, DBG_MMA_ACC, acc);
+#ifdef MOE_DEBUG_LOG
+          if (kPair) {
+            const Task& t0 = p.tasks[2 * u];
+            const Task& t1 = p.tasks[2 * u + 1];
+            if (!DBG_CHECK(p, t0.kind == t1.kind && t0.n == t1.n && t0.e == t1.e, 10, u, t0.kind * 16 + t1.kind,
+                           t0.n * 4096 + t1.n))
+              break;
+          }
+#endif
+          if (!DBG_CHECK(p, (tmem & 0xFFFFu) + acc * ACC_COLS + ACC_COLS <= (uint32_t)TMEM_COLS && (tmem >> 16) == 0,
+                         11, tmem, acc, u))
+            break;
           {
+            DBG_SET(p, DBG_MMA_WAIT, 1);
             TRACE_T0();
-            if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.status, p.timeout_ns)) break;
+            if (!wait_bar(&tempty[acc], acc_phase ^ 1u)) break;
             TRACE_ADD(p, TR_MMA_TEMPTY);
+            DBG_SET(p, DBG_MMA_WAIT, 0);
           }
           tc_fence_after();
           const uint32_t d = tmem + acc * ACC_COLS;
           for (int kb = 0; kb < nk; ++kb) {
             {
+              DBG_SET(p, DBG_MMA_WAIT, 2);
               TRACE_T0();
-              if (!mbar_wait(&full[stage], phase, p.status, p.timeout_ns)) { ok = false; break; }
+              if (!wait_bar(&full[stage], phase)) { ok = false; break; }
               TRACE_ADD(p, TR_MMA_FULL);
+              DBG_SET(p, DBG_MMA_WAIT, 0);
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + stage * STAGE_STRIDE);
+            const uint32_t a_addr = smem_u32(smem + stage * G::stride);
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
-            if (mx) {
-              // scales -> TMEM (in order with the MMAs below), then four 32-wide K blocks
-              const uint32_t sf = a_addr + STAGE_BYTES;
-              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
-              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
-              tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_mxf8_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
-                            idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
-                            tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
-            } else {
+            if constexpr (kPair) {
 #pragma unroll
               for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                            (kb | kk) != 0 ? 1u : 0u);
+                mma_bf16_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+              mma_commit_pair(&empty[stage], 0x3);
+            } else {
+              if (mx) {
+                // scales -> TMEM (in order with the MMAs below), then four 32-wide K blocks
+                const uint32_t sf = a_addr + STAGE_BYTES;
+                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
+                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
+                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_mxf8_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
+                              idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
+                              tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                  mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+              }
+              mma_commit(&empty[stage]);
             }
-            mma_commit(&empty[stage]);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+#ifdef MOE_DEBUG_LOG
+            DBG_SET(p, DBG_MMA_STAGES, ++mma_stages);
+#endif
+            if (++stage == NST) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          mma_commit(&tfull[acc]);
+          if constexpr (kPair) mma_commit_pair(&tfull[acc], 0x3);
+          else mma_commit(&tfull[acc]);
           if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
         }
-        mma_commit(drain);
-        mbar_wait(drain, 0, p.status, p.timeout_ns);
+        if constexpr (kPair) mma_commit_pair(drain, 0x1);
+        else mma_commit(drain);
+        wait_bar(drain, 0);
         TRACE_FLUSH(p);
       }
       __syncwarp();
@@ -697,14 +864,20 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
       const int row = q * 32 + lane;
       uint32_t acc = 0, acc_phase = 0;
       bool routed_done = false;
+      const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
       TRACE_LOCALS();
-      for (int ti = cta; ti < n_tasks; ti += p.n_gemm) {
+      for (int u = walk.first; u < walk.n_units; u += walk.step) {
+        const int ti = walk.task(u);
         const Task t = p.tasks[ti];
         // one thread waits and decides for all four warps, so that they agree
         // on stopping and never strand each other at the named barrier
         if (threadIdx.x == 64) {
+          DBG_SET(p, DBG_EPI_UNIT, u);
+          DBG_SET(p, DBG_EPI_TASK, ti);
+          DBG_SET(p, DBG_EPI_WAIT, 1);
           TRACE_T0();
-          int ok = mbar_wait(&tfull[acc], acc_phase, p.status, p.timeout_ns) ? 1 : 0;
+          int ok = wait_bar(&tfull[acc], acc_phase) ? 1 : 0;
+          DBG_SET(p, DBG_EPI_WAIT, 0);
           if (ok && t.kind == TASK_S2 && !routed_done)  // the combine reads every routed output row
             ok = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
           routed_done = routed_done || (ok && t.kind == TASK_S2);
@@ -714,25 +887,50 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
         named_bar_sync(1, 128);
         if (*s_ok == 0) break;
         TRACE_T0();
+        if (threadIdx.x == 64 && u + walk.step < walk.n_units) {
+          // the next task's combine reads k staging rows per token once: bring
+          // them into L2 one epilogue ahead (a hint only; lines written later
+          // by other CTAs are updated in L2)
+          const Task nt = p.tasks[walk.task(u + walk.step)];
+          if (nt.kind == TASK_S2) {  // one contiguous block: rows x k x 256 fp16
+            const uint8_t* y0 = reinterpret_cast<const uint8_t*>(p.Y + y_offset(p, nt.out_row, 0, nt.n));
+            const uint32_t bytes = (uint32_t)nt.rows * p.k * BN_DOWN * 2;
+            for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(y0 + o, min(65536u, bytes - o));
+          }
+        }
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
         const int r0 = q * 32;                        // the warp's first tile row
-        const int nrows = min(32, max(0, t.rows - r0));  // its valid rows
+        int nrows = min(32, max(0, t.rows - r0));  // its valid rows
+#ifdef MOE_DEBUG_LOG
+        {
+          const bool col_ok = (tmem & 0xFFFFu) + acc * ACC_COLS + ACC_COLS <= (uint32_t)TMEM_COLS;
+          bool rows_ok = true;
+          if (t.kind == TASK_R1) rows_ok = t.out_row + r0 + nrows <= p.slots * p.b;
+          else if (t.kind == TASK_S1 || t.kind == TASK_S2) rows_ok = t.out_row + r0 + nrows <= p.T;
+          else {
+            const int jj = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
+            rows_ok = t.p0 + t.rows <= p.R && jj >= 0 && jj < p.R &&
+                      y_offset(p, jj / p.k, jj % p.k, t.n) + BN_DOWN <= (size_t)p.n_chunks * BM * p.k * p.D;
+          }
+          if (!DBG_CHECK(p, col_ok, 20, tmem, acc, ti) || !DBG_CHECK(p, rows_ok, 21 + t.kind, t.out_row, r0, ti))
+            nrows = 0;
+        }
+#endif
         EpiStage& st = epi[q];
+        const AccRelease rel{&tempty[acc], tempty_even + acc * 8u, kPair};
         if (t.kind == TASK_R1 && p.mx) {
           epilogue_swiglu_mx(taddr, reinterpret_cast<uint8_t*>(p.ring_h) + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
-                             p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows,
-                             &tempty[acc]);
+                             p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows, rel);
         } else if (t.kind == TASK_R1) {
-          epilogue_swiglu(taddr, st, p.ring_h + (size_t)(t.out_row + r0) * p.I + t.n * BN_UP, p.I, nrows, &tempty[acc]);
+          epilogue_swiglu(taddr, st, p.ring_h + (size_t)(t.out_row + r0) * p.I + t.n * BN_UP, p.I, nrows, rel);
         } else if (t.kind == TASK_S1) {
-          epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows,
-                          &tempty[acc]);
+          epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows, rel);
         } else if (t.kind == TASK_R2) {
           const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
-          epilogue_copy_f16(taddr, st, p.Y, p.D, t.n * BN_DOWN, j, nrows, &tempty[acc]);
+          epilogue_copy_f16(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
         } else {
-          epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, &tempty[acc]);
+          epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, rel);
         }
         // h tiles are read back by TMA (async proxy); Y and out only by plain loads
         if (t.kind == TASK_R1 || t.kind == TASK_S1) fence_proxy_async_global();
@@ -743,6 +941,7 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
           TRACE_SET(p, TR_TASKS, ti);
           if (t.done0 >= 0) red_release_add_gpu(p.counters + t.done0, 1);
           if (t.done1 >= 0) red_release_add_gpu(p.counters + t.done1, 1);
+          DBG_SET(p, DBG_EPI_DONE, u);
         }
         if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
       }
@@ -750,9 +949,15 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 3);
+    // pairs: neither CTA frees TMEM or leaves while the other may still issue
+    // into its TMEM, arrive on its barriers or load into its shared memory
+    if constexpr (kPair) cluster_sync_all();
+    if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 4);
     if (warp == 1) {
       tc_fence_after();
-      tmem_dealloc(tmem, TMEM_COLS);
+      if constexpr (kPair) tmem_dealloc_pair(tmem, TMEM_COLS);
+      else tmem_dealloc(tmem, TMEM_COLS);
     }
   }
 
@@ -770,24 +975,69 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0) TRACE_SET(p, TR_END_NS, globaltimer_ns());
+  if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 5);
+}
+
+__global__ void __launch_bounds__(MEGA_THREADS, 1)
+    moe_megakernel(const __grid_constant__ TensorMaps maps, const FwdParams p) {
+  mega_body<false>(maps, p);
+}
+
+// CTA pairs: launched with a cluster of 2 (ranks 0/1 of a cluster form a pair)
+__global__ void __launch_bounds__(MEGA_THREADS, 1)
+    moe_megakernel_pair(const __grid_constant__ TensorMaps maps, const FwdParams p) {
+  mega_body<true>(maps, p);
 }
 
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(moe_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MEGA_SMEM_BYTES);
+  const bool pair = p.pair != 0;
+  const void* fn = pair ? reinterpret_cast<const void*>(moe_megakernel_pair)
+                        : reinterpret_cast<const void*>(moe_megakernel);
+  const int smem = pair ? MegaGeom<true>::smem_bytes : MegaGeom<false>::smem_bytes;
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(MEGA_THREADS);
-  cfg.dynamicSmemBytes = MEGA_SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pair ? 2 : 1;
+  if (pair) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair, maps, p);
   return cudaLaunchKernelEx(&cfg, moe_megakernel, maps, p);
 }
 
-int megakernel_smem_bytes() { return MEGA_SMEM_BYTES; }
+int megakernel_smem_bytes() { return MegaGeom<false>::smem_bytes; }
+
+// CTAs of the pair kernel that can be resident at once (clusters of 2, one CTA per SM)
+int megakernel_pair_max_ctas() {
+  const int smem = MegaGeom<true>::smem_bytes;
+  if (cudaFuncSetAttribute(moe_megakernel_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms & ~1));
+  cfg.blockDim = dim3(MEGA_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, moe_megakernel_pair, &cfg) != cudaSuccess) return -1;
+  return 2 * clusters;
+}
 
 }  // namespace moe

@@ -1,0 +1,142 @@
+// Test hook: one tcgen05.mma.cta_group::2 tile on a CTA pair, used by the GPU
+// tests to pin the pair encodings (TMEM allocation for two CTAs, TMA loads
+// counted on the even CTA's mbarrier, M = 256 instruction descriptor, the
+// split of A and B over the two shared memories, the multicast commit and the
+// rows of D each CTA's TMEM receives) against a CPU reference.  Not part of
+// the forward path.
+//
+// D [256, 256] fp32 = A [256, 64] B [256, 64]^T, A and B bf16 row-major (K
+// contiguous).  CTA r of the pair loads A rows [128 r, 128 r + 128) and B rows
+// [128 r, 128 r + 128); the even CTA issues four M = 256, N = 256, K = 16 MMAs;
+// CTA r then writes D rows [128 r, 128 r + 128) from its own TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr uint64_t kProbeWaitNs = 2000000000ull;  // 2 s per wait
+
+template <bool kCluster>
+__device__ bool probe_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kProbeWaitNs) return false;
+  }
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    pair_probe_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, float* D,
+                      int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;          // 128 rows x 128 B (64 bf16), 128-byte swizzle
+  uint8_t* sB = smem + 16384;  // 128 rows x 128 B
+  __shared__ __align__(8) uint64_t full;
+  __shared__ __align__(8) uint64_t done;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    mbar_init(&full, 1);
+    mbar_init(&done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair<256>(&tmem_slot);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (threadIdx.x == 0) {
+    const uint32_t full_even = mapa_shared(&full, rank & ~1u);
+    if ((rank & 1u) == 0) mbar_arrive_expect_tx(&full, 2u * 32768u);  // both CTAs' A and B halves
+    tma_load_2d_pair(sA, &mA, full_even, 0, (int)(128 * rank));
+    tma_load_2d_pair(sB, &mB, full_even, 0, (int)(128 * rank));
+    if ((rank & 1u) == 0) {
+      if (probe_wait<true>(&full, 0)) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(256, 256);
+        const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                        kk > 0 ? 1u : 0u);
+        mma_commit_pair(&done, 0x3);
+      } else {
+        atomicExch(status, 1);
+      }
+    }
+  }
+  __syncwarp();
+  const bool ok = probe_wait<true>(&done, 0);
+  tc_fence_after();
+  if (ok) {
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int c = 0; c < 256; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem + lane_base + c, r);
+      tmem_ld_wait();
+      for (int j = 0; j < 32; ++j) D[(size_t)(128 * rank + row) * 256 + c + j] = __uint_as_float(r[j]);
+    }
+  } else if (lane == 0) {
+    atomicExch(status + 1 + rank, 1);
+  }
+  tc_fence_before();
+  cluster_sync_all();  // no CTA frees TMEM or leaves while the other may still touch it
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 256);
+  }
+}
+
+}  // namespace moe
+
+namespace {
+
+typedef CUresult (*probe_encode_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode_probe_map(probe_encode_fn enc, CUtensorMap* m, const void* ptr) {
+  cuuint64_t dims[2] = {64, 256};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? 0
+             : -1;
+}
+
+}  // namespace
+
+extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, void* stream) {
+  if (!A || !B || !D || !status) return -1;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return -1;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return -4;
+  CUtensorMap mA, mB;
+  if (encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mA, A) ||
+      encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mB, B))
+    return -1;
+  const int smem = 32 * 1024 + 1024;
+  if (cudaFuncSetAttribute(moe::pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -4;
+  moe::pair_probe_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(mA, mB, D, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
 // minibatch's segments are contiguous, so the whole layout comes from
 // per-expert counts and block-wide scans (no serial walk).
 // p.segs holds [segments x 4] {e, mt_begin, mt_count, m}.
-// Dynamic shared memory: mb_tiles[n_mb], mt_first[n_mb], step_off[n_mb + lag + 1].
+// Dynamic shared memory: see sched_dyn_ints.
 
 // exclusive scan of v[0..n) in place (shared memory), returns the total; all threads call it
 __device__ int block_exclusive_scan(int* v, int n, int* warp_tmp) {
@@ -185,32 +185,42 @@ __device__ __forceinline__ void piece_rows(const int* sS, int e, int m, int b, i
 __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   __shared__ int s_seg[E_MAX];  // per expert: segment count, then first segment
   __shared__ int s_mt[E_MAX];   // per expert: M-tile count, then first M-tile
+  __shared__ int s_mtp[E_MAX];  // per expert: task slots per column tile (M-tiles, padded to pairs), then first
   __shared__ int s_tmp[SCHED_THREADS / 32];
   __shared__ int s_tot[4];
   const int E = p.E, b = p.b, n_mb = p.n_mb, tid = threadIdx.x;
-  int* mb_tiles = dsm;
-  int* mt_first = dsm + n_mb;
-  int* step_off = dsm + 2 * n_mb;
+  int* mb_tiles = dsm;             // per minibatch: M-tiles
+  int* mt_first = dsm + n_mb;      // ... first M-tile
+  int* mb_ptiles = dsm + 2 * n_mb;  // ... task slots per column tile (= mb_tiles without pairs)
+  int* mtp_first = dsm + 3 * n_mb;  // ... first task slot
+  int* step_off = dsm + 4 * n_mb;
   const int n_steps = n_mb + p.lag;
+  // CTA pairs take two consecutive tasks on the same weight tile: a segment's
+  // M-tile count is rounded up to even, the extra task being an empty partner
+  auto padded = [&](int cnt) { return p.pair ? (cnt + 1) & ~1 : cnt; };
 
-  for (int m = tid; m < n_mb; m += blockDim.x) mb_tiles[m] = 0;
+  for (int m = tid; m < n_mb; m += blockDim.x) mb_tiles[m] = mb_ptiles[m] = 0;
   if (tid < E) {
-    int nseg = 0, ntile = 0;
+    int nseg = 0, ntile = 0, nptile = 0;
     if (sS[tid + 1] > sS[tid]) {
       const int m0 = sS[tid] / b, m1 = (sS[tid + 1] - 1) / b;
       nseg = m1 - m0 + 1;
       for (int m = m0; m <= m1; ++m) {
         int a, z;
         piece_rows(sS, tid, m, b, a, z);
-        ntile += (z - a + BM - 1) / BM;
+        const int cnt = (z - a + BM - 1) / BM;
+        ntile += cnt;
+        nptile += padded(cnt);
       }
     }
     s_seg[tid] = nseg;
     s_mt[tid] = ntile;
+    s_mtp[tid] = nptile;
   }
   __syncthreads();
   const int nseg_tot = block_exclusive_scan(s_seg, E, s_tmp);
   const int nmt_tot = block_exclusive_scan(s_mt, E, s_tmp);
+  block_exclusive_scan(s_mtp, E, s_tmp);
   const bool fits = nseg_tot <= p.n_mb + E && nmt_tot <= p.n_mtiles_max;
   if (tid == 0 && !fits) raise_status(p.status, STATUS_SCHEDULE_INVALID);
 
@@ -231,14 +241,19 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   }
   if (fits && tid < E && sS[tid + 1] > sS[tid]) {
     const int m0 = sS[tid] / b, m1 = (sS[tid + 1] - 1) / b;
-    int mt = s_mt[tid];
+    int mt = s_mt[tid], mtp = s_mtp[tid];
     for (int m = m0; m <= m1; ++m) {
       int a, z;
       piece_rows(sS, tid, m, b, a, z);
       const int cnt = (z - a + BM - 1) / BM;
-      if (a == m * b) mt_first[m] = mt;  // exactly one segment opens each minibatch
+      if (a == m * b) {  // exactly one segment opens each minibatch
+        mt_first[m] = mt;
+        mtp_first[m] = mtp;
+      }
       atomicAdd(&mb_tiles[m], cnt);
+      atomicAdd(&mb_ptiles[m], padded(cnt));
       mt += cnt;
+      mtp += padded(cnt);
     }
   }
   __syncthreads();
@@ -253,12 +268,13 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
     }
   }
   for (int s = tid; s < n_steps; s += blockDim.x) {
-    const int r1 = s < n_mb ? mb_tiles[s] * p.N1 : 0;
-    const int r2 = s - p.lag >= 0 ? mb_tiles[s - p.lag] * p.N2 : 0;
+    const int r1 = s < n_mb ? mb_ptiles[s] * p.N1 : 0;
+    const int r2 = s - p.lag >= 0 ? mb_ptiles[s - p.lag] * p.N2 : 0;
     step_off[s] = r1 + r2;
   }
   __syncthreads();
-  const int n_s1 = p.N1s * p.n_smtiles, n_s2 = p.N2s * p.n_smtiles;
+  const int n_st = padded(p.n_smtiles);  // shared-expert token tiles, padded to pairs
+  const int n_s1 = p.N1s * n_st, n_s2 = p.N2s * n_st;
   const int routed = block_exclusive_scan(step_off, n_steps, s_tmp);
   const long long total = (long long)n_s1 + routed + n_s2;
   if (tid == 0) {
@@ -276,27 +292,31 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   __syncthreads();
   if (!s_tot[0]) return;
 
-  // shared-expert tasks: tiles of 128 tokens, column tile major
+  // shared-expert tasks: tiles of 128 tokens, token-tile major (with pairs:
+  // token-tile-pair major, the pair's two tiles side by side per column tile)
   for (int q = blockIdx.x * blockDim.x + tid; q < n_s1 + n_s2; q += gridDim.x * blockDim.x) {
     const bool down = q >= n_s1;
     const int qq = down ? q - n_s1 : q;
     const int nn = down ? p.N2s : p.N1s;
-    const int mt = qq / nn;  // token-tile major, as for the routed segments
+    const int mt = p.pair ? 2 * (qq / (2 * nn)) + (qq & 1) : qq / nn;
+    const int n = p.pair ? (qq >> 1) % nn : qq % nn;
+    const bool real = mt < p.n_smtiles;
+    const int mtr = real ? mt : mt - 1;  // an empty partner reads its partner's rows
     Task tk;
     tk.kind = down ? TASK_S2 : TASK_S1;
-    tk.n = qq % nn;
+    tk.n = n;
     tk.e = 0;
-    tk.a_row = mt * BM;
-    tk.rows = min(BM, p.T - mt * BM);
-    tk.p0 = mt * BM;
-    tk.out_row = mt * BM;
-    tk.dep0 = down ? ctr_shready(p, mt) : -1;
-    tk.need0 = down ? p.N1s : 0;
+    tk.a_row = mtr * BM;
+    tk.rows = real ? min(BM, p.T - mt * BM) : 0;
+    tk.p0 = mtr * BM;
+    tk.out_row = mtr * BM;
+    tk.dep0 = down && real ? ctr_shready(p, mt) : -1;
+    tk.need0 = down && real ? p.N1s : 0;
     tk.dep1 = -1;
     tk.need1 = 0;
-    tk.done0 = down ? -1 : ctr_shready(p, mt);
+    tk.done0 = !down && real ? ctr_shready(p, mt) : -1;
     tk.done1 = -1;
-    tk.mt = mt;
+    tk.mt = mtr;
     tk.pad[0] = tk.pad[1] = 0;
     store_task(p.tasks + (down ? (int)total - n_s2 + qq : qq), tk);
   }
@@ -305,31 +325,37 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     if (sS[e + 1] <= sS[e]) continue;
     const int m0 = sS[e] / b, m1 = (sS[e + 1] - 1) / b;
-    int mtb = s_mt[e];
+    int mtb = s_mt[e], ptb = s_mtp[e];
     for (int m = m0; m <= m1; ++m) {
       int a, z;
       piece_rows(sS, e, m, b, a, z);
       const int cnt = (z - a + BM - 1) / BM;
+      const int cntp = padded(cnt);
       const int slot_row = (m % p.slots) * b;
-      const int r1_base = n_s1 + step_off[m] + p.N1 * (mtb - mt_first[m]);
+      const int r1_base = n_s1 + step_off[m] + p.N1 * (ptb - mtp_first[m]);
       const int sr2 = m + p.lag;
       const int r2_base =
-          n_s1 + step_off[sr2] + (sr2 < n_mb ? mb_tiles[sr2] * p.N1 : 0) + p.N2 * (mtb - mt_first[m]);
+          n_s1 + step_off[sr2] + (sr2 < n_mb ? mb_ptiles[sr2] * p.N1 : 0) + p.N2 * (ptb - mtp_first[m]);
       const int need_h = m >= p.slots ? mb_tiles[m - p.slots] * p.N2 : 0;
-      for (int q = tid; q < cnt * (p.N1 + p.N2); q += blockDim.x) {
-        const bool down = q >= cnt * p.N1;
-        const int qq = down ? q - cnt * p.N1 : q;
-        const int i = qq % cnt;  // column-tile major: the segment's tiles share a weight slice
-        const int r0 = a + i * BM;
+      for (int q = tid; q < cntp * (p.N1 + p.N2); q += blockDim.x) {
+        const bool down = q >= cntp * p.N1;
+        const int qq = down ? q - cntp * p.N1 : q;
+        const int i = qq % cntp;  // column-tile major: the segment's tiles share a weight slice
+        const bool real = i < cnt;
+        const int ir = real ? i : i - 1;  // an empty partner reads its partner's rows
+        const int r0 = a + ir * BM;
         Task tk;
         tk.kind = down ? TASK_R2 : TASK_R1;
-        tk.n = qq / cnt;
+        tk.n = qq / cntp;
         tk.e = e;
         tk.a_row = slot_row + (r0 - m * b);
-        tk.rows = min(BM, z - r0);
+        tk.rows = real ? min(BM, z - r0) : 0;
         tk.p0 = r0;
         tk.out_row = tk.a_row;
-        if (!down) {
+        if (!real) {
+          tk.dep0 = tk.dep1 = tk.done0 = tk.done1 = -1;
+          tk.need0 = tk.need1 = 0;
+        } else if (!down) {
           tk.dep0 = p.direct ? -1 : ctr_filled(p, m);  // direct dispatch: x itself is the A operand
           tk.need0 = p.G;
           tk.dep1 = m >= p.slots ? ctr_r2(p, m - p.slots) : -1;
@@ -344,7 +370,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           tk.done0 = ctr_r2(p, m);
           tk.done1 = ctr_ydone();
         }
-        tk.mt = mtb + i;
+        tk.mt = mtb + ir;
         tk.pad[0] = tk.pad[1] = 0;
         store_task(p.tasks + (down ? r2_base : r1_base) + qq, tk);
       }
@@ -356,11 +382,16 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
         mr[3] = m;
       }
       mtb += cnt;
+      ptb += cntp;
     }
   }
 }
 
-int schedule_smem_bytes(const FwdParams& p) { return (int)sizeof(int) * (3 * p.n_mb + p.lag + 1); }
+// dynamic shared memory of build_tasks: mb_tiles, mt_first, mb_ptiles and
+// mtp_first [n_mb] each, then step_off [n_mb + lag + 1]
+__host__ __device__ inline int sched_dyn_ints(int n_mb, int lag) { return 4 * n_mb + (n_mb + lag + 1); }
+
+int schedule_smem_bytes(const FwdParams& p) { return (int)sizeof(int) * sched_dyn_ints(p.n_mb, p.lag); }
 
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream) {
   const int smem = schedule_smem_bytes(p);

@@ -1,0 +1,81 @@
+"""The CTA-pair flavour of the persistent kernel (mma_pair = 1: each expert
+tile is one tcgen05.mma.cta_group::2 over two 128-row M-tiles that share the
+weight tile) against the fp64 oracle, with the same bars as the one-CTA
+kernel: routing and schedule bit-exact, outputs within rel-L2 1e-2 and
+max-abs 3e-2 rms, repeated runs and scheduling knobs bitwise identical.
+
+The cases cover segments with an odd number of M-tiles (the pair's second
+task is an empty partner), a single token, a ragged token tail, no shared
+expert, one expert taking every token and the full-size DSV3 workload."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from test_gpu_parity import _full_size, run_and_check, small
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from routing_grouped_expert_gemm_gb300 import build
+    build.build()
+
+
+def test_pair_tiny_workload_all_tokens():
+    run_and_check(mi.make_inputs("tiny"), minibatch=512, ring_slots=2, gather_ctas=2, mma_pair=1)
+
+
+def test_pair_medium_ragged_tokens_and_tiles():
+    run_and_check(small(1000, 512, 256, 32, 6, 256), minibatch=1024, ring_slots=3, gather_ctas=4, mma_pair=1)
+
+
+@pytest.mark.parametrize("T", [1, 129, 300])
+def test_pair_edge_token_counts(T):
+    inp = small(384, 256, 128, 16, 4, 128, cid=301)
+    run_and_check(inp, T=T, minibatch=128, ring_slots=2, gather_ctas=2, mma_pair=1)
+
+
+def test_pair_no_shared_expert_softmax():
+    run_and_check(small(384, 512, 256, 24, 5, 0, score="softmax", cid=302, beta_scale=0.0), minibatch=512,
+                  gather_ctas=2, mma_pair=1)
+
+
+def test_pair_one_expert_takes_every_token():
+    inp = small(640, 256, 128, 16, 3, 128, cid=304)
+    inp.b_router[7] = 40.0
+    _, _, res = run_and_check(inp, minibatch=256, ring_slots=2, gather_ctas=2, mma_pair=1)
+    assert res["expert_counts"].cpu().numpy()[7] == 640
+
+
+def test_pair_bitwise_deterministic_across_knobs():
+    import gpu_util as g
+    inp = small(1000, 512, 256, 32, 6, 256, cid=307)
+    x = g.to_dev_bf16(inp.x)
+    outs = []
+    for kw in (dict(minibatch=1024, ring_slots=3, gather_ctas=4, lag=1),
+               dict(minibatch=1024, ring_slots=3, gather_ctas=4, lag=1),
+               dict(minibatch=128, ring_slots=2, gather_ctas=2, lag=1),
+               dict(minibatch=256, ring_slots=1, gather_ctas=8, lag=0),
+               dict(minibatch=8192, ring_slots=1, gather_ctas=2, lag=0, gemm_ctas=20),
+               dict(minibatch=512, ring_slots=5, gather_ctas=16, lag=1, gemm_ctas=6)):
+        layer = g.Layer(inp, mma_pair=1, **kw)
+        res = layer.run(x, poison=True)
+        assert res["status"] == 0
+        outs.append((kw, res["out"].view(torch.int16).cpu().numpy()))
+    for kw, o in outs[1:]:
+        assert np.array_equal(o, outs[0][1]), f"output bits differ for {kw}"
+
+
+def test_pair_rejects_unsupported_modes():
+    import routing_grouped_expert_gemm_gb300 as rg
+    for kw in (dict(precision="mxfp8"), dict(dispatch="direct"), dict(gather_ctas=3)):
+        with pytest.raises(rg.MoEError):
+            rg.moe_plan_create(256, 256, 128, 16, 4, 128, mma_pair=1, **kw)
+
+
+def test_pair_full_size_dsv3_zipf_sampled():
+    _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)
