@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 sub-measurement")
     ap.add_argument("--gather-ctas-mx", type=int, default=6, help="gather CTAs for the MXFP8 layer")
     ap.add_argument("--dispatch", choices=["ring", "direct"], default="ring")
+    ap.add_argument("--mma-pair", type=int, default=0, choices=[0, 1],
+                    help="BF16 layer: CTA-pair (cta_group::2) expert tiles")
+    ap.add_argument("--raster", type=int, default=0, help="up/gate tile order: M-tiles per group (0 = default)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: a smaller case with this many tokens (uniform routing)")
     ap.add_argument("--experts", type=int, default=0,
@@ -225,11 +228,53 @@ def workload_config(shape, args, extra=None):
            "score": shape.score, "load": "Zipf(1.1) via router bias" if shape.load == "zipf" else shape.load,
            "precision": shape.precision, "minibatch": args.minibatch, "ring_slots": args.ring_slots,
            "gather_ctas": args.gather_ctas, "lag": args.lag, "dispatch": args.dispatch,
+           "mma_pair": args.mma_pair if shape.precision == "bf16" else 0, "raster": args.raster,
            "l2": "inputs larger than L2 (expert weights 22.5 GB, x 235 MB for dsv3); no flush",
            "parallelism": "replicas"}
     if extra:
         cfg["note"] = extra
     return cfg
+
+
+# ----------------------------------------------------------------------------- recorded DRAM traffic
+def kernel_sources_hash() -> str:
+    """sha256 over the CUDA sources and the C header: a recorded ncu traffic figure
+    applies only to the kernels it was taken from."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "routing_grouped_expert_gemm_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    files.append(os.path.join(root, "include", "moe.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(key: str, cfg: dict):
+    """dram__bytes_read.sum + dram__bytes_write.sum of one persistent-kernel
+    launch, from profiles/traffic_<key>.txt, if it was taken from these sources
+    and this launch configuration; else None."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", f"traffic_{key}.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split(None, 1)
+            if len(parts) == 2 and not line.startswith("#"):
+                rec[parts[0]] = parts[1].strip()
+    if rec.get("sources_sha256") != kernel_sources_hash():
+        return None
+    for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch"):
+        if k in rec and str(cfg.get(k)) != rec[k]:
+            return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -246,7 +291,8 @@ class Runner:
                                        ring_slots=args.ring_slots,
                                        gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8"
                                        else args.gather_ctas,
-                                       lag=args.lag, dispatch=args.dispatch)
+                                       lag=args.lag, dispatch=args.dispatch, raster=args.raster,
+                                       mma_pair=args.mma_pair if shape.precision == "bf16" else 0)
         w = {"W_router": dev(inp.w_router),
              "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()}
         for name, arr, rows, K in (("W_up", inp.w_up, shape.E * shape.I, shape.D),
@@ -375,6 +421,8 @@ def run_ours(args, world, rank, local):
     peak = mx_peak if shape.precision == "mxfp8" else bf16_peak
     mega_mean = sum(res["mega_ms"]) / len(res["mega_ms"])
     achieved = flops / (mega_mean / 1000.0) / 1e12
+    cfg = workload_config(shape, args)
+    traffic = recorded_traffic(f"{shape.name}_{shape.precision}", cfg)
     line = {
         "metric": METRIC,
         "value": replica_throughput(world, T, args.steps, elapsed_ms), "unit": "tokens/s", "n_gpus": world,
@@ -382,13 +430,16 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.precision == "bf16" else "mxfp8 (e4m3 + e8m0) routed, bf16 shared",
         "data": "synthetic (seeded normal inputs, random-init weights)",
-        "config": workload_config(shape, args),
+        "config": cfg,
         "tflops": world * flops * args.steps / (elapsed_ms / 1000.0) / 1e12,
         "ms_median_step": statistics.median(res["step_ms"]),
         "phases_ms_mean": {"router_topk": statistics.mean(res["router_ms"]),
                            "schedule": statistics.mean(res["sched_ms"]), "megakernel": mega_mean},
         "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "traffic_note": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum, "
+                                     "profiles/traffic_%s_%s.txt)" % (shape.name, shape.precision)
+                                     if traffic else "no ncu capture for these sources and this config",
                      "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)"
                                     + (", x2 for MXFP8" if shape.precision == "mxfp8" else ""),
                      "frac_of_burst_peak": achieved / (float(peaks["bf16_tflops"])

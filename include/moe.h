@@ -96,6 +96,12 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe
  *              a segment with an odd number of M-tiles pads its last pair.
  *              bf16 precision with ring dispatch only (MOE_ERR_INVALID_ARG
  *              otherwise); gather_ctas must be even.  0: one CTA per tile.
+ *   raster     order of an expert segment's up/gate tiles: groups of `raster`
+ *              M-tiles, each group sweeping all I/128 column tiles (so a
+ *              group's token rows are re-read from L2 while its weight
+ *              slices stream); 0 = the library default, >= the segment's
+ *              M-tile count = column-tile major over the whole segment.  With
+ *              mma_pair it is rounded up to even.  Results do not depend on it.
  * Zero for minibatch / ring_slots / gather_ctas / lag picks the defaults
  * (8192 / 4 / 8 / 1).
  */
@@ -117,7 +123,7 @@ typedef struct moe_config {
   int32_t dispatch;
   int32_t l2_prefetch;
   int32_t mma_pair;
-  int32_t reserved[1];
+  int32_t raster;
 } moe_config;
 
 /*

@@ -154,7 +154,10 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.minibatch < BM || c.minibatch > 32768 || c.minibatch % BM) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c.ring_slots < c.lag + 1 || c.ring_slots > 64) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((c.T_max * c.k + c.minibatch - 1) / c.minibatch > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;  // schedule smem
+  if (c.raster < 0) return MOE_ERR_INVALID_ARG;
+  if (c.raster == 0) c.raster = 1 << 20;  // default: column-tile major over the whole segment
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
+  if (c.mma_pair) c.raster = (c.raster + 1) & ~1;  // a pair's two tasks share a column tile
   if (c.mma_pair && (c.precision != MOE_PREC_BF16 || c.dispatch != MOE_DISPATCH_RING || (c.gather_ctas & 1) ||
                      (c.gemm_ctas & 1)))
     return MOE_ERR_INVALID_ARG;
@@ -263,6 +266,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.mx = mx ? 1 : 0;
   p.direct = c.dispatch == MOE_DISPATCH_DIRECT ? 1 : 0;
   p.pair = c.mma_pair;
+  p.raster = c.raster;
   p.b = c.minibatch;
   p.slots = c.ring_slots;
   p.G = c.gather_ctas;

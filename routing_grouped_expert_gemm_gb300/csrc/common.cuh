@@ -78,6 +78,7 @@ struct FwdParams {
   int mx;               // routed experts in MXFP8 (1) or BF16 (0)
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
   int pair;             // 1: GEMM CTAs run as pairs, tasks 2i and 2i + 1 share one cta_group::2 MMA
+  int raster;           // M-tiles per group of a segment's up/gate tiles (column tiles swept per group)
   int b, slots, G, n_gemm, lag;
   int n_mb, R;          // minibatches, routes (T*k)
   int N1, N2, N1s, N2s; // column tiles: I/128, D/256, I_s/128, D/256
@@ -127,7 +128,8 @@ struct FwdParams {
 enum : int {
   TR_START_NS = 0, TR_END_NS, TR_PROD_DEP, TR_PROD_EMPTY, TR_MMA_FULL, TR_MMA_TEMPTY, TR_EPI_TFULL, TR_EPI_BUSY,
   TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_EPI_R1, TR_EPI_R2, TR_EPI_S1, TR_EPI_S2,
-  TRACE_SLOTS = 16
+  TR_TMA_LAT_NS /* stage issue -> full barrier seen by the MMA issuer, summed */, TR_TMA_STAGES,
+  TRACE_SLOTS = 18
 };
 // Each thread that times anything keeps its sums in registers (TRACE_LOCALS)
 // and adds them to the CTA's slots once, at the end (TRACE_FLUSH), so the
@@ -260,6 +262,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     }
   }
   return true;
+}
+
+// Waiting for this CTA's own asynchronous copies or MMAs before it frees
+// their resources or exits: the status word is not consulted (work already
+// issued always completes), only the time limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > (uint64_t)limit_ns) return false;
+  return true;
+}
+// after an abort (status raised), a bounded pause so that copies other CTAs of
+// a pair issued into this CTA's shared memory have landed before it exits
+__device__ __forceinline__ void settle_after_abort(const int* status) {
+  if (ld_relaxed_gpu(status) == 0) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
 }
 
 // the same for a phase completed with the help of the other CTA of a pair

@@ -40,6 +40,8 @@ __device__ __forceinline__ uint8_t* align_1024_mk(uint8_t* p) {
 }
 
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
+constexpr int GATHER_BUFS = 16;          // row buffers of a gather CTA (BF16 ring)
+constexpr int GATHER_STORES = 4;         // row stores a gather CTA keeps in flight
 constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
 
 // ------------------------------------------------------------------ MXFP8 helpers
@@ -102,11 +104,69 @@ __device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, 
     *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = __ldg(sw + kg);
 }
 
-__device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
+// BF16 ring through the TMA engine: one thread streams the CTA's rows of a
+// minibatch through nbuf shared-memory row buffers (bulk load x row ->
+// buffer -> bulk store to the ring), keeping nbuf - GATHER_STORES loads and
+// up to GATHER_STORES stores in flight: the buffer of row i + ahead is the one
+// row i - GATHER_STORES used, refilled once that row's store has finished
+// reading it.  row_seq counts rows over the whole kernel (buffer = row_seq %
+// nbuf, its mbarrier phase = (row_seq / nbuf) & 1).  Returns false if a load
+// did not land within the time limit.
+__device__ bool gather_rows_bulk(const FwdParams& p, int lo, int r0, int r1, size_t slot_base, uint8_t* buf,
+                                 uint64_t* gbar, int nbuf, uint32_t& row_seq) {
+  const uint32_t row_bytes = (uint32_t)p.D * 2u;
+  const int n = r1 - r0;
+  const int ahead = nbuf - GATHER_STORES;
+  auto load = [&](int i) {
+    const uint32_t q = row_seq + (uint32_t)i;
+    const int b = (int)(q % (uint32_t)nbuf);
+    const int t = p.sched[(size_t)(r0 + i) * 3];
+    mbar_arrive_expect_tx(&gbar[b], row_bytes);
+    bulk_load(buf + (size_t)b * row_bytes, p.x + (size_t)t * p.D, row_bytes, &gbar[b]);
+  };
+  int loaded = min(ahead, n);
+  for (int i = 0; i < loaded; ++i) load(i);
+  bool ok = true;
+  int i = 0;
+  for (; i < n; ++i) {
+    const uint32_t q = row_seq + (uint32_t)i;
+    const int b = (int)(q % (uint32_t)nbuf);
+    if (!mbar_wait(&gbar[b], (q / (uint32_t)nbuf) & 1u, p.status, p.timeout_ns)) {
+      ok = false;
+      break;
+    }
+    bulk_store(p.ring_x + (slot_base + (size_t)(r0 + i - lo)) * p.D, buf + (size_t)b * row_bytes, row_bytes);
+    bulk_commit_group();
+    if (i + ahead < n) {
+      bulk_wait_group_read<GATHER_STORES>();  // rows <= i - GATHER_STORES are done reading their buffers
+      load(i + ahead);
+      ++loaded;
+    }
+  }
+  // aborted: the loads issued but not yet consumed land before the buffers are left
+  for (; i < loaded; ++i) {
+    const uint32_t q = row_seq + (uint32_t)i;
+    mbar_wait_drain(&gbar[q % (uint32_t)nbuf], (q / (uint32_t)nbuf) & 1u, p.timeout_ns);
+  }
+  bulk_wait_group_all();
+  row_seq += (uint32_t)loaded;
+  return ok;
+}
+
+__device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* buf, int buf_bytes, uint64_t* gbar) {
   TRACE_LOCALS();
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // BF16: row buffers for the bulk-copy path (every row fits: D <= 8192)
+  const int nbuf = min(GATHER_BUFS, buf_bytes / (p.D * 2));  // >= 12 for D <= 8192
+  uint32_t row_seq = 0;
+  if (!p.mx && threadIdx.x == 0) {
+    for (int i = 0; i < nbuf; ++i) mbar_init(&gbar[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   for (int m = 0; m < p.n_mb; ++m) {
+    if (threadIdx.x == 0) *s_flag = 1;
     if (m >= p.slots) {
       if (threadIdx.x == 0) {
         const int need = p.meta[META_MB + 4 * (m - p.slots)];
@@ -132,17 +192,23 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag) {
                              p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
         }
       }
-    } else {  // contiguous row ranges per CTA, rows strided over its warps
+    } else {  // contiguous row ranges per CTA
       const int hi = min(p.R, lo + p.b);
       const int per = (hi - lo + p.G - 1) / p.G;
       const int r0 = lo + g * per, r1 = min(hi, r0 + per);
-      for (int r = r0 + warp; r < r1; r += nwarps) {
-        const int t = p.sched[(size_t)r * 3];
-        gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + (slot_base + (size_t)(r - lo)) * p.D);
+      if (nbuf > GATHER_STORES) {  // one thread drives the TMA engine
+        if (threadIdx.x == 0 && r1 > r0)
+          *s_flag = gather_rows_bulk(p, lo, r0, r1, slot_base, buf, gbar, nbuf, row_seq) ? 1 : 0;
+      } else {  // rows strided over the warps, copied through registers
+        for (int r = r0 + warp; r < r1; r += nwarps) {
+          const int t = p.sched[(size_t)r * 3];
+          gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + (slot_base + (size_t)(r - lo)) * p.D);
+        }
       }
     }
     fence_proxy_async_global();
     __syncthreads();
+    if (*s_flag == 0) break;  // a bulk load gave up: the minibatch is not complete
     if (threadIdx.x == 0) {
       TRACE_ADD(p, TR_GATHER_BUSY);
       red_release_add_gpu(p.counters + ctr_filled(p, m), 1);
@@ -564,6 +630,9 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = s_flag + 1;
   EpiStage* epi = reinterpret_cast<EpiStage*>(smem + NST * G::stride + 256);
+#ifdef MOE_TRACE
+  volatile uint64_t* s_issue_ns = bars + 24;  // per stage: when its loads were issued (trace builds)
+#endif
   // MXFP8 needs TMEM columns for the scales: one accumulator buffer instead of two
   const uint32_t n_acc = p.mx ? 1u : 2u;
 
@@ -574,7 +643,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   const bool has_shared = p.N1s > 0;
 
   if (is_gather) {
-    gather_role(p, s_flag);
+    // the stage buffers hold rows in flight; the barriers live in the (unused) epilogue staging area
+    gather_role(p, s_flag, smem, NST * G::stride, reinterpret_cast<uint64_t*>(epi));
     __syncthreads();
   } else {
     const int cta = blockIdx.x - p.G;
@@ -691,6 +761,9 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           uint8_t* ssf = sa + STAGE_BYTES;
           // a K step is 64 bf16 or 128 E4M3 elements: 128 bytes per row either way
           const int kc = kb * (mx ? BK_MX : BK);
+#ifdef MOE_TRACE
+          if (lead_lane) s_issue_ns[stage] = globaltimer_ns();
+#endif
           if constexpr (kPair) {
             if (lead_lane) {
               if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)PAIR_STAGE_BYTES);
@@ -764,7 +837,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       // for the even one at the cluster barrier below)
       if (lead_lane && leader)
         for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
-          wait_bar(&full[i % NST], (uint32_t)(i / NST) & 1u);
+          mbar_wait_drain(&full[i % NST], (uint32_t)(i / NST) & 1u, p.timeout_ns);
       if (lead_lane) TRACE_FLUSH(p);
       __syncwarp();
     } else if (warp == 1) {
@@ -811,6 +884,10 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               TRACE_T0();
               if (!wait_bar(&full[stage], phase)) { ok = false; break; }
               TRACE_ADD(p, TR_MMA_FULL);
+#ifdef MOE_TRACE
+              _trv[TR_TMA_LAT_NS] += globaltimer_ns() - s_issue_ns[stage];
+              _trv[TR_TMA_STAGES] += 1;
+#endif
               DBG_SET(p, DBG_MMA_WAIT, 0);
             }
             tc_fence_after();
@@ -854,7 +931,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         }
         if constexpr (kPair) mma_commit_pair(drain, 0x1);
         else mma_commit(drain);
-        wait_bar(drain, 0);
+        mbar_wait_drain(drain, 0, p.timeout_ns);  // every MMA issued has completed before TMEM is freed
         TRACE_FLUSH(p);
       }
       __syncwarp();
@@ -947,6 +1024,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       }
       if (threadIdx.x == 64) TRACE_FLUSH(p);
     }
+    if constexpr (kPair) settle_after_abort(p.status);
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 3);

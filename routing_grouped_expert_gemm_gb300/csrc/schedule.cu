@@ -340,13 +340,22 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
       for (int q = tid; q < cntp * (p.N1 + p.N2); q += blockDim.x) {
         const bool down = q >= cntp * p.N1;
         const int qq = down ? q - cntp * p.N1 : q;
-        const int i = qq % cntp;  // column-tile major: the segment's tiles share a weight slice
+        int i, n;
+        if (down) {  // column-tile major: the segment's tiles share a weight slice
+          i = qq % cntp;
+          n = qq / cntp;
+        } else {  // groups of p.raster M-tiles, each sweeping the column tiles
+          const int grp = qq / (p.raster * p.N1), within = qq % (p.raster * p.N1);
+          const int gc = min(p.raster, cntp - grp * p.raster);  // M-tiles in this group
+          i = grp * p.raster + within % gc;
+          n = within / gc;
+        }
         const bool real = i < cnt;
         const int ir = real ? i : i - 1;  // an empty partner reads its partner's rows
         const int r0 = a + ir * BM;
         Task tk;
         tk.kind = down ? TASK_R2 : TASK_R1;
-        tk.n = qq / cntp;
+        tk.n = n;
         tk.e = e;
         tk.a_row = slot_row + (r0 - m * b);
         tk.rows = real ? min(BM, z - r0) : 0;

@@ -121,6 +121,8 @@ def test_bitwise_deterministic_across_knobs():
                dict(minibatch=256, ring_slots=1, gather_ctas=8, lag=0),
                dict(minibatch=8192, ring_slots=1, gather_ctas=2, lag=0, gemm_ctas=20),
                dict(minibatch=512, ring_slots=5, gather_ctas=16, lag=1, gemm_ctas=7),
+               dict(minibatch=1024, ring_slots=3, gather_ctas=4, raster=1),
+               dict(minibatch=512, ring_slots=4, gather_ctas=4, raster=3),
                dict(minibatch=1024, ring_slots=3, dispatch="direct"),
                dict(minibatch=128, ring_slots=1, lag=0, dispatch="direct", gemm_ctas=11)):
         layer = g.Layer(inp, **kw)
