@@ -58,7 +58,7 @@ typedef enum moe_device_status {
 
 typedef enum moe_score_fn { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_fn;
 typedef enum moe_precision { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precision;
-typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe_dispatch;
+typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_DISPATCH_SPREAD = 2 } moe_dispatch;
 
 /*
  * Layer shape and execution knobs.
@@ -79,7 +79,11 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1 } moe
  *              ring of minibatches (the pages' communication SMs);
  *              MOE_DISPATCH_DIRECT: the GEMM CTAs' TMA producers fetch each
  *              tile's token rows straight from x (tile::gather4), no gather
- *              CTAs and no x ring (MXFP8: x is quantised once per token first)
+ *              CTAs and no x ring (MXFP8: x is quantised once per token first);
+ *              MOE_DISPATCH_SPREAD: the same ring as MOE_DISPATCH_RING, filled
+ *              by two otherwise idle warps of every GEMM CTA (each takes the
+ *              minibatch's M-tiles c, c + gemm CTAs, ...), so every SM runs
+ *              expert tiles; gather_ctas is ignored
  *   gather_ctas  ring dispatch: CTAs (one per SM) that only gather tokens, >= 1
  *              (Sec. 3.4 "Computation-Communication SM Tuning"); ignored for
  *              direct dispatch

@@ -34,7 +34,7 @@ MOE_ROUTE_STATIC_MAX_TOKENS = 16384
 MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID = 0, 1, 2
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_PREC_BF16, MOE_PREC_MXFP8 = 0, 1
-MOE_DISPATCH_RING, MOE_DISPATCH_DIRECT = 0, 1
+MOE_DISPATCH_RING, MOE_DISPATCH_DIRECT, MOE_DISPATCH_SPREAD = 0, 1, 2
 
 
 class MoEError(RuntimeError):
@@ -154,7 +154,7 @@ def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precis
     if isinstance(precision, str):
         precision = {"bf16": MOE_PREC_BF16, "mxfp8": MOE_PREC_MXFP8}[precision]
     if isinstance(dispatch, str):
-        dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT}[dispatch]
+        dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT, "spread": MOE_DISPATCH_SPREAD}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
                      lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster)
     h = ctypes.c_void_p()

@@ -136,7 +136,8 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (!cfg_in || !out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   moe_config c = *cfg_in;
-  if (c.dispatch != MOE_DISPATCH_RING && c.dispatch != MOE_DISPATCH_DIRECT) return MOE_ERR_INVALID_ARG;
+  if (c.dispatch != MOE_DISPATCH_RING && c.dispatch != MOE_DISPATCH_DIRECT && c.dispatch != MOE_DISPATCH_SPREAD)
+    return MOE_ERR_INVALID_ARG;
   if (c.minibatch == 0) c.minibatch = 8192;
   if (c.ring_slots == 0) c.ring_slots = 4;
   if (c.gather_ctas == 0 && c.dispatch == MOE_DISPATCH_RING) c.gather_ctas = 8;
@@ -158,7 +159,8 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.raster == 0) c.raster = 1 << 20;  // default: column-tile major over the whole segment
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
   if (c.mma_pair) c.raster = (c.raster + 1) & ~1;  // a pair's two tasks share a column tile
-  if (c.mma_pair && (c.precision != MOE_PREC_BF16 || c.dispatch != MOE_DISPATCH_RING || (c.gather_ctas & 1) ||
+  if (c.dispatch == MOE_DISPATCH_SPREAD) c.gather_ctas = 0;  // the GEMM CTAs' spare warps gather
+  if (c.mma_pair && (c.precision != MOE_PREC_BF16 || c.dispatch == MOE_DISPATCH_DIRECT || (c.gather_ctas & 1) ||
                      (c.gemm_ctas & 1)))
     return MOE_ERR_INVALID_ARG;
   if (c.dispatch == MOE_DISPATCH_DIRECT) c.gather_ctas = 0;  // the GEMM producers gather
@@ -265,12 +267,14 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.score_fn = c.score_fn;
   p.mx = mx ? 1 : 0;
   p.direct = c.dispatch == MOE_DISPATCH_DIRECT ? 1 : 0;
+  p.spread = c.dispatch == MOE_DISPATCH_SPREAD ? 1 : 0;
   p.pair = c.mma_pair;
   p.raster = c.raster;
   p.b = c.minibatch;
   p.slots = c.ring_slots;
   p.G = c.gather_ctas;
   p.n_gemm = pl->grid - c.gather_ctas;
+  p.gparts = p.spread ? p.n_gemm : c.gather_ctas;
   p.lag = c.lag;
   p.n_mb = (int)L.n_mb;
   p.R = (int)L.R;
@@ -303,9 +307,9 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.tasks = reinterpret_cast<Task*>(ws + L.tasks);
   p.ring_x = reinterpret_cast<bf16*>(ws + L.ring_x);
   p.ring_h = reinterpret_cast<bf16*>(ws + L.ring_h);
-  p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
   p.xq = mx ? ws + L.xq : nullptr;
   p.xs = mx ? ws + L.xs : nullptr;
+  p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
   p.sfh = mx ? ws + L.sfh : nullptr;
   p.w_up_sf = mx ? w->W_up_scale : nullptr;
   p.w_gate_sf = mx ? w->W_gate_scale : nullptr;

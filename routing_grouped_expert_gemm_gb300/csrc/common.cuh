@@ -78,6 +78,8 @@ struct FwdParams {
   int mx;               // routed experts in MXFP8 (1) or BF16 (0)
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
   int pair;             // 1: GEMM CTAs run as pairs, tasks 2i and 2i + 1 share one cta_group::2 MMA
+  int spread;           // 1: two spare warps of every GEMM CTA fill the ring (no gather CTAs)
+  int gparts;           // parts the ring fill of a minibatch is split into (gather CTAs or GEMM CTAs)
   int raster;           // M-tiles per group of a segment's up/gate tiles (column tiles swept per group)
   int b, slots, G, n_gemm, lag;
   int n_mb, R;          // minibatches, routes (T*k)
@@ -108,7 +110,7 @@ struct FwdParams {
   bf16* ring_x;       // [slots*b, D] (MXFP8: E4M3 codes, 1 byte each)
   bf16* ring_h;       // [slots*b, I] (MXFP8: E4M3 codes)
   uint8_t* sfx;       // MXFP8 ring dispatch: scale blocks of the gathered x, [n_mtiles_max][D/128][512 B]
-  uint8_t* xq;        // MXFP8 direct dispatch: x quantised once per token, [T, D] E4M3
+  uint8_t* xq;        // MXFP8: x quantised once per token, [T, D] E4M3 (gathered into the ring, or read directly)
   uint8_t* xs;        // ... and its E8M0 scales, [T, D/32] row-major
   uint8_t* sfh;       // MXFP8: scale blocks of h, [n_mtiles_max][I/128][512 B]
   const uint8_t* w_up_sf;    // MXFP8 weight scale blocks (moe_quantize_mxfp8 layout)
@@ -129,7 +131,8 @@ enum : int {
   TR_START_NS = 0, TR_END_NS, TR_PROD_DEP, TR_PROD_EMPTY, TR_MMA_FULL, TR_MMA_TEMPTY, TR_EPI_TFULL, TR_EPI_BUSY,
   TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_EPI_R1, TR_EPI_R2, TR_EPI_S1, TR_EPI_S2,
   TR_TMA_LAT_NS /* stage issue -> full barrier seen by the MMA issuer, summed */, TR_TMA_STAGES,
-  TRACE_SLOTS = 18
+  TR_GATHER_LOADWAIT /* bulk gather: waiting for a row load */, TR_GATHER_STOREWAIT /* ... for stores to drain */,
+  TRACE_SLOTS = 20
 };
 // Each thread that times anything keeps its sums in registers (TRACE_LOCALS)
 // and adds them to the CTA's slots once, at the end (TRACE_FLUSH), so the
@@ -307,7 +310,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + __expf(-v)); }
+// SiLU(v) = v / (1 + e^-v) with the fast exponential and reciprocal intrinsics
+// (for v -> -inf the reciprocal of +inf is 0, so the result tends to -0)
+__device__ __forceinline__ float silu_f32(float v) { return v * __fdividef(1.0f, 1.0f + __expf(-v)); }
 
 // OCP MX v1.0, MXFP8 E4M3 block of 32: X = 2^(floor(log2 amax) - 8), codes =
 // E4M3(v / X) rounded to nearest-even and saturated at +-448; an all-zero block
@@ -321,15 +326,22 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint32_t* q) {
     for (int i = 0; i < 8; ++i) q[i] = 0;
     return 0;
   }
-  int se = ilogbf(amax) - 8;
+  // floor(log2 amax) from the exponent field (a subnormal amax has none)
+  const uint32_t eb = (__float_as_uint(amax) >> 23) & 0xFFu;
+  int se = (eb != 0u ? (int)eb - 127 : ilogbf(amax)) - 8;
   se = max(-127, min(127, se));
+  // v * 2^-se, exact (|result| < 2^9) when 2^-se is a normal float, as ldexpf
+  const bool pow2 = se >= -126 && se <= 126;
+  const float scale = __uint_as_float((uint32_t)(127 - se) << 23);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t w = 0;
+    float a[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      w |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[4 * i + j], -se), __NV_SATFINITE, __NV_E4M3) << (8 * j);
-    q[i] = w;
+    for (int j = 0; j < 4; ++j) a[j] = pow2 ? v[4 * i + j] * scale : ldexpf(v[4 * i + j], -se);
+    // two codes per conversion; element 4i + j lands in byte j of the word
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a[0], a[1]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a[2], a[3]), __NV_SATFINITE, __NV_E4M3);
+    q[i] = lo | (hi << 16);
   }
   return (uint32_t)(se + 127);
 }

@@ -40,8 +40,9 @@ __device__ __forceinline__ uint8_t* align_1024_mk(uint8_t* p) {
 }
 
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
-constexpr int GATHER_BUFS = 16;          // row buffers of a gather CTA (BF16 ring)
+constexpr int GATHER_BUFS = 32;          // row buffers of a gather CTA (at most)
 constexpr int GATHER_STORES = 4;         // row stores a gather CTA keeps in flight
+constexpr int GATHER_TOK_CHUNK = 4096;   // rows whose tokens a gather CTA stages in shared memory at a time
 constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
 
 // ------------------------------------------------------------------ MXFP8 helpers
@@ -76,13 +77,13 @@ __device__ void gather_copy_row(const FwdParams& p, const bf16* src_row, bf16* d
   }
 }
 
-// MXFP8: x was quantised once per token before this kernel (codes xq [T, D],
-// scales xs [T, D/32]); the gather copies a token's codes into the ring and
-// its scale words (one per 128-wide K step) into the tile's scale blocks.
+// MXFP8: a token's E4M3 codes into a ring row (the warp's lanes copy 16-byte
+// vectors, the whole row in flight) and its E8M0 words into the M-tile's
+// scale blocks (one word per 128-wide K step, row r_in_tile of the tile)
 __device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, uint8_t* sf_tile, int r_in_tile) {
   const int lane = threadIdx.x & 31;
-  const int nv = p.D / 16;  // 16-byte vectors of codes
-  constexpr int UNR = 16;   // D <= 8192 in one pass
+  const int nv = p.D / 16;
+  constexpr int UNR = 16;  // D <= 8192 in one pass
   const uint4* src = reinterpret_cast<const uint4*>(p.xq + (size_t)t * p.D);
   uint4* dst = reinterpret_cast<uint4*>(dst_row);
   for (int base = 0; base < nv; base += 32 * UNR) {
@@ -104,26 +105,66 @@ __device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, 
     *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = __ldg(sw + kg);
 }
 
-// BF16 ring through the TMA engine: one thread streams the CTA's rows of a
-// minibatch through nbuf shared-memory row buffers (bulk load x row ->
-// buffer -> bulk store to the ring), keeping nbuf - GATHER_STORES loads and
+// Ring fill spread over the GEMM CTAs (MOE_DISPATCH_SPREAD): warps 6 and 7
+// of GEMM CTA `part` (of `parts`) copy the rows of the minibatch's M-tiles
+// part, part + parts, ... through registers, while the CTA's other warps run
+// expert tiles; every part adds 1 to the minibatch's fill counter.  They sync
+// among themselves with named barrier 2 (64 threads).
+__device__ void gather_role_spread(const FwdParams& p, int part, int parts, volatile int* s_gflag) {
+  const int w = (threadIdx.x >> 5) - 6;  // 0 or 1
+  const bool lead = threadIdx.x == 6 * 32;
+  for (int m = 0; m < p.n_mb; ++m) {
+    if (m >= p.slots) {  // ring slot m % slots free again: minibatch m - slots' up/gate tiles are done
+      if (lead)
+        *s_gflag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), p.meta[META_MB + 4 * (m - p.slots)],
+                                   p.status, p.timeout_ns) ? 1 : 0;
+      named_bar_sync(2, 64);
+      if (*s_gflag == 0) break;
+    }
+    const int lo = m * p.b;
+    const size_t slot_base = (size_t)(m % p.slots) * p.b;
+    const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
+    for (int i = part; i < ntile; i += parts) {
+      const int mt = mt0 + i;
+      const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
+      for (int r = w; r < rows; r += 2) {
+        const int t = p.sched[(size_t)(p0 + r) * 3];
+        const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
+        if (p.mx)
+          gather_copy_row_mx(p, t, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
+                             p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
+        else
+          gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + ring_row * p.D);
+      }
+    }
+    fence_proxy_async_global();  // the ring rows are read by TMA
+    named_bar_sync(2, 64);
+    if (lead) red_release_add_gpu(p.counters + ctr_filled(p, m), 1);
+  }
+}
+
+// The ring through the TMA engine: one thread streams the CTA's rows of a
+// minibatch (bf16 x rows, or MXFP8 E4M3 code rows of the per-token quantised
+// x) through nbuf shared-memory row buffers (bulk load -> buffer -> bulk store
+// to the ring), keeping nbuf - GATHER_STORES loads and
 // up to GATHER_STORES stores in flight: the buffer of row i + ahead is the one
 // row i - GATHER_STORES used, refilled once that row's store has finished
 // reading it.  row_seq counts rows over the whole kernel (buffer = row_seq %
 // nbuf, its mbarrier phase = (row_seq / nbuf) & 1).  Returns false if a load
 // did not land within the time limit.
-__device__ bool gather_rows_bulk(const FwdParams& p, int lo, int r0, int r1, size_t slot_base, uint8_t* buf,
-                                 uint64_t* gbar, int nbuf, uint32_t& row_seq) {
-  const uint32_t row_bytes = (uint32_t)p.D * 2u;
+__device__ bool gather_rows_bulk(const FwdParams& p, const uint8_t* src, uint8_t* dst, uint32_t row_bytes, int lo,
+                                 int r0, int r1, const int* tok, size_t slot_base, uint8_t* buf, uint64_t* gbar,
+                                 int nbuf, uint32_t& row_seq) {
   const int n = r1 - r0;
   const int ahead = nbuf - GATHER_STORES;
   auto load = [&](int i) {
     const uint32_t q = row_seq + (uint32_t)i;
     const int b = (int)(q % (uint32_t)nbuf);
-    const int t = p.sched[(size_t)(r0 + i) * 3];
+    const int t = tok[i];  // row r0 + i's token, from the shared table
     mbar_arrive_expect_tx(&gbar[b], row_bytes);
-    bulk_load(buf + (size_t)b * row_bytes, p.x + (size_t)t * p.D, row_bytes, &gbar[b]);
+    bulk_load(buf + (size_t)b * row_bytes, src + (size_t)t * row_bytes, row_bytes, &gbar[b]);
   };
+  TRACE_LOCALS();
   int loaded = min(ahead, n);
   for (int i = 0; i < loaded; ++i) load(i);
   bool ok = true;
@@ -131,14 +172,21 @@ __device__ bool gather_rows_bulk(const FwdParams& p, int lo, int r0, int r1, siz
   for (; i < n; ++i) {
     const uint32_t q = row_seq + (uint32_t)i;
     const int b = (int)(q % (uint32_t)nbuf);
-    if (!mbar_wait(&gbar[b], (q / (uint32_t)nbuf) & 1u, p.status, p.timeout_ns)) {
+    TRACE_T0();
+    const bool landed = mbar_wait(&gbar[b], (q / (uint32_t)nbuf) & 1u, p.status, p.timeout_ns);
+    TRACE_ADD(p, TR_GATHER_LOADWAIT);
+    if (!landed) {
       ok = false;
       break;
     }
-    bulk_store(p.ring_x + (slot_base + (size_t)(r0 + i - lo)) * p.D, buf + (size_t)b * row_bytes, row_bytes);
+    bulk_store(dst + (slot_base + (size_t)(r0 + i - lo)) * row_bytes, buf + (size_t)b * row_bytes, row_bytes);
     bulk_commit_group();
     if (i + ahead < n) {
-      bulk_wait_group_read<GATHER_STORES>();  // rows <= i - GATHER_STORES are done reading their buffers
+      {
+        TRACE_T0();
+        bulk_wait_group_read<GATHER_STORES>();  // rows <= i - GATHER_STORES are done reading their buffers
+        TRACE_ADD(p, TR_GATHER_STOREWAIT);
+      }
       load(i + ahead);
       ++loaded;
     }
@@ -148,19 +196,28 @@ __device__ bool gather_rows_bulk(const FwdParams& p, int lo, int r0, int r1, siz
     const uint32_t q = row_seq + (uint32_t)i;
     mbar_wait_drain(&gbar[q % (uint32_t)nbuf], (q / (uint32_t)nbuf) & 1u, p.timeout_ns);
   }
-  bulk_wait_group_all();
+  {
+    TRACE_T0();
+    bulk_wait_group_all();
+    TRACE_ADD(p, TR_GATHER_STOREWAIT);
+  }
+  TRACE_FLUSH(p);
   row_seq += (uint32_t)loaded;
   return ok;
 }
 
-__device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* buf, int buf_bytes, uint64_t* gbar) {
+__device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* buf, int buf_bytes, uint64_t* gbar,
+                            int* tok) {
   TRACE_LOCALS();
   const int g = blockIdx.x;
-  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  // BF16: row buffers for the bulk-copy path (every row fits: D <= 8192)
-  const int nbuf = min(GATHER_BUFS, buf_bytes / (p.D * 2));  // >= 12 for D <= 8192
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5, lane = threadIdx.x & 31;
+  // a ring row: D bf16, or D E4M3 codes
+  const uint32_t row_bytes = (uint32_t)p.D * (p.mx ? 1u : 2u);
+  const uint8_t* src = p.mx ? p.xq : reinterpret_cast<const uint8_t*>(p.x);
+  uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_x);
+  const int nbuf = min(GATHER_BUFS, buf_bytes / (int)row_bytes);  // >= 12 for D <= 8192
   uint32_t row_seq = 0;
-  if (!p.mx && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     for (int i = 0; i < nbuf; ++i) mbar_init(&gbar[i], 1);
     fence_barrier_init();
   }
@@ -180,29 +237,41 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* b
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
     TRACE_T0();
-    if (p.mx) {  // whole M-tiles per CTA: a tile's scale blocks are written by one CTA
+    // contiguous row ranges per CTA for the rows themselves
+    const int hi = min(p.R, lo + p.b);
+    const int per = (hi - lo + p.G - 1) / p.G;
+    const int r0 = lo + g * per, r1 = min(hi, r0 + per);
+    if (warp == 0) {
+      // the rows' tokens go to a shared table first (32 lanes, independent
+      // loads), so the issuing lane never waits on a global load per row
+      bool ok = true;
+      for (int c0 = r0; c0 < r1 && ok; c0 += GATHER_TOK_CHUNK) {
+        const int c1 = min(r1, c0 + GATHER_TOK_CHUNK);
+        for (int i = lane; i < c1 - c0; i += 32) tok[i] = p.sched[(size_t)(c0 + i) * 3];
+        __syncwarp();
+        int okl = 1;
+        if (lane == 0)
+          okl = gather_rows_bulk(p, src, dst, row_bytes, lo, c0, c1, tok, slot_base, buf, gbar, nbuf, row_seq) ? 1
+                                                                                                               : 0;
+        ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+        __syncwarp();
+      }
+      if (lane == 0 && !ok) *s_flag = 0;
+    } else if (p.mx) {
+      // MXFP8: the other warps put the tokens' E8M0 words into the scale
+      // blocks of the minibatch's M-tiles g, g + G, ... (one word per row and
+      // 128-wide K step)
       const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
+      const int nkg = p.D / BK_MX;
       for (int i = g; i < ntile; i += p.G) {
         const int mt = mt0 + i;
         const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
-        for (int r = warp; r < rows; r += nwarps) {
+        uint8_t* sf_tile = p.sfx + (size_t)mt * nkg * SF_BLOCK_BYTES;
+        for (int r = warp - 1; r < rows; r += nwarps - 1) {
           const int t = p.sched[(size_t)(p0 + r) * 3];
-          const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
-          gather_copy_row_mx(p, t, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
-                             p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
-        }
-      }
-    } else {  // contiguous row ranges per CTA
-      const int hi = min(p.R, lo + p.b);
-      const int per = (hi - lo + p.G - 1) / p.G;
-      const int r0 = lo + g * per, r1 = min(hi, r0 + per);
-      if (nbuf > GATHER_STORES) {  // one thread drives the TMA engine
-        if (threadIdx.x == 0 && r1 > r0)
-          *s_flag = gather_rows_bulk(p, lo, r0, r1, slot_base, buf, gbar, nbuf, row_seq) ? 1 : 0;
-      } else {  // rows strided over the warps, copied through registers
-        for (int r = r0 + warp; r < r1; r += nwarps) {
-          const int t = p.sched[(size_t)r * 3];
-          gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + (slot_base + (size_t)(r - lo)) * p.D);
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.xs + (size_t)t * (p.D / 32));
+          for (int kg = lane; kg < nkg; kg += 32)
+            *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r, 0)) = __ldg(sw + kg);
         }
       }
     }
@@ -261,9 +330,9 @@ __device__ __forceinline__ int task_nk(const FwdParams& p, int kind) {
 
 // MXFP8 scale blocks of a K step: A (the tile's rows), then B's two 128-row halves
 __device__ __forceinline__ void mx_scale_sources(const FwdParams& p, const Task& t, int kb, const uint8_t** src) {
-  if (t.kind == TASK_R1) {
+  if (t.kind == TASK_R1) {  // direct dispatch: src[0] unused (the producer lanes write the A block)
     const int nkg = p.D / BK_MX;
-    src[0] = p.sfx + ((size_t)t.mt * nkg + kb) * SF_BLOCK_BYTES;
+    src[0] = p.sfx ? p.sfx + ((size_t)t.mt * nkg + kb) * SF_BLOCK_BYTES : nullptr;
     const size_t wb = ((size_t)(t.e * p.I + t.n * BN_UP) / BM * nkg + kb) * SF_BLOCK_BYTES;
     src[1] = p.w_up_sf + wb;
     src[2] = p.w_gate_sf + wb;
@@ -409,18 +478,19 @@ __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf
 }
 
 // routed down-projection tile -> fp16 staging rows (route j = t k + slot from
-// the schedule table); y_mine: offset of this thread's row's 256-column segment
-__device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, long long y_mine, int nrows,
-                                  const AccRelease& rel) {
+// the schedule table), restaged through shared memory so that every warp
+// store covers 4 rows x 64 contiguous bytes; y_mine: offset of this thread's
+// row's 256-column segment.  The buffer is handed back after the last TMEM
+// read (with two accumulator buffers the MMA issuer rarely waits for it).
+__device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y, long long y_mine, int nrows,
+                                         const AccRelease& rel) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < BN_DOWN; c += 32) {
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
-    if (c + 32 == BN_DOWN) {
-      release_acc(rel);
-    }
+    if (c + 32 == BN_DOWN) release_acc(rel);
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -435,6 +505,29 @@ __device__ void epilogue_copy_f16(uint32_t taddr, EpiStage& st, __half* Y, long 
       }
     }
     __syncwarp();
+  }
+}
+
+// The same with the buffer held as briefly as possible (single-buffered
+// MXFP8 tiles): thread r owns TMEM lane r = tile row r, whose 256
+// outputs form one contiguous 512-byte staging segment at y_row: every 16
+// columns read from TMEM go straight out as one full 32-byte sector, and the
+// buffer is handed back right after the last read.
+__device__ void epilogue_copy_f16(uint32_t taddr, __half* y_row, bool valid, const AccRelease& rel) {
+#pragma unroll
+  for (int c = 0; c < BN_DOWN; c += 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr + (uint32_t)c, r);
+    tmem_ld_wait();
+    if (c + 16 == BN_DOWN) release_acc(rel);
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h[j] = pack_f16x2_sat(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    if (valid) {
+      uint4* d = reinterpret_cast<uint4*>(y_row + c);
+      d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
   }
 }
 
@@ -605,6 +698,27 @@ __device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
   }
 }
 
+// Accumulator buffer of each task.  The two TMEM buffers alternate, except
+// that routed MXFP8 tasks always take buffer 0: their block scales sit in the
+// first columns of buffer 1.  Shared-expert tasks (which come before and after
+// every routed task) alternate in MXFP8 layers too.  Per-buffer use counts
+// give the mbarrier parities; the MMA issuer and the epilogue walk the same
+// tasks, so they pick the same buffers.
+struct AccSeq {
+  uint32_t uses0 = 0u, uses1 = 0u;  // scalars, not an array: no local memory
+  uint32_t alt = 0u;
+  __device__ __forceinline__ uint32_t next(bool mx_task) {
+    const uint32_t b = mx_task ? 0u : alt;
+    if (!mx_task) alt ^= 1u;
+    return b;
+  }
+  __device__ __forceinline__ uint32_t uses(uint32_t b) const { return b ? uses1 : uses0; }
+  __device__ __forceinline__ void used(uint32_t b) {
+    if (b) ++uses1;
+    else ++uses0;
+  }
+};
+
 // Task walk: a GEMM CTA takes units first, first + step, ...; a unit is one
 // task, or with CTA pairs two consecutive tasks (2u: even CTA, 2u + 1: odd CTA)
 // that share one weight tile.
@@ -633,8 +747,6 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 #ifdef MOE_TRACE
   volatile uint64_t* s_issue_ns = bars + 24;  // per stage: when its loads were issued (trace builds)
 #endif
-  // MXFP8 needs TMEM columns for the scales: one accumulator buffer instead of two
-  const uint32_t n_acc = p.mx ? 1u : 2u;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
@@ -644,7 +756,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 
   if (is_gather) {
     // the stage buffers hold rows in flight; the barriers live in the (unused) epilogue staging area
-    gather_role(p, s_flag, smem, NST * G::stride, reinterpret_cast<uint64_t*>(epi));
+    gather_role(p, s_flag, smem, NST * G::stride, reinterpret_cast<uint64_t*>(epi),
+                reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(epi) + GATHER_BUFS));
     __syncthreads();
   } else {
     const int cta = blockIdx.x - p.G;
@@ -722,16 +835,19 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         const Operands o = task_operands(maps, p, t);
         const bool mx = task_is_mx(p, t.kind);
         const bool gather_a = p.direct && t.kind == TASK_R1;
+        // MXFP8 direct dispatch: the lanes write the A scale block (the tile's
+        // 128 tokens' E8M0 words of this K step) into shared memory themselves
+        const bool sf_lanes = gather_a && mx;
         // pairs: this CTA's half of B -- up (even) or gate (odd) rows for
         // GEMM1, the first or second 128 output columns for GEMM2
         const CUtensorMap* bmap_pair = o.b1 ? (walk.rank ? o.b1 : o.b0) : o.b0;
         const int brow_pair = o.b1 ? o.b_row : o.b_row + 128 * walk.rank;
-        // direct dispatch: lane l fetches tile rows 4l .. 4l+3 (rows past the
-        // tile's end repeat its first token: discarded rows, in-bounds reads)
+        // lane l handles tile rows 4l .. 4l+3 (rows past the tile's end repeat
+        // its first token: discarded rows, in-bounds reads)
         int tok[4] = {0, 0, 0, 0};
         uint32_t sfw[4][4];  // MXFP8: scale words of the 4 rows, 4 K steps ahead
         const int nkg = p.D / BK_MX;
-        if (gather_a) {
+        if (gather_a || sf_lanes) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int r = 4 * lane + j;
@@ -772,9 +888,10 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
             }
           } else {
-            if (gather_a) {
+            if (gather_a)
               tma_gather4(sa + lane * 4 * 128, &maps.x_rows, &full[stage], kc, tok[0], tok[1], tok[2], tok[3]);
-              if (mx) {  // the tile's A scale block, written here rather than copied
+            {
+              if (sf_lanes) {  // the tile's A scale block, written here rather than copied
                 const int d = kb & 3;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -801,7 +918,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
             if (lead_lane) {
               // bytes the TMA engine delivers (the scale block written above is not counted)
               const uint32_t tx = (mx ? (uint32_t)MX_STAGE_TX : (uint32_t)STAGE_BYTES) -
-                                  (gather_a && mx ? (uint32_t)SF_BLOCK_BYTES : 0u);
+                                  (sf_lanes ? (uint32_t)SF_BLOCK_BYTES : 0u);
               mbar_arrive_expect_tx(&full[stage], tx);
               if (!gather_a) tma_load_2d(sa, o.a, &full[stage], kc, t.a_row);
               if (o.b1) {
@@ -813,7 +930,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               if (mx) {
                 const uint8_t* src[3];
                 mx_scale_sources(p, t, kb, src);
-                for (int i = gather_a ? 1 : 0; i < 3; ++i)
+                for (int i = sf_lanes ? 1 : 0; i < 3; ++i)
                   bulk_load(ssf + i * SF_BLOCK_BYTES, src[i], SF_BLOCK_BYTES, &full[stage]);
               }
               // L2 prefetch of the tiles p.l2_prefetch K steps ahead: the loads that
@@ -846,7 +963,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         TRACE_LOCALS();
         const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, 256);
         const uint32_t idesc_mx = idesc_mxf8_e4m3(BM, 256);
-        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        uint32_t stage = 0, phase = 0;
+        AccSeq accs;
         bool ok = true;
 #ifdef MOE_DEBUG_LOG
         int mma_stages = 0;
@@ -855,6 +973,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           const int kind = p.tasks[walk.task(u)].kind;
           const bool mx = task_is_mx(p, kind);
           const int nk = task_nk(p, kind);
+          const uint32_t acc = accs.next(mx);
           DBG_SET(p, DBG_MMA_UNIT, u);
           DBG_SET(p, DBG_MMA_ACC, acc);
 #ifdef MOE_DEBUG_LOG
@@ -872,7 +991,9 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           {
             DBG_SET(p, DBG_MMA_WAIT, 1);
             TRACE_T0();
-            if (!wait_bar(&tempty[acc], acc_phase ^ 1u)) break;
+            if (!wait_bar(&tempty[acc], (accs.uses(acc) & 1u) ^ 1u)) break;
+            // MXFP8: the block scales go to buffer 1's first columns, which its last user must have released
+            if (mx && accs.uses1 > 0 && !wait_bar(&tempty[1], (accs.uses1 & 1u) ^ 1u)) break;
             TRACE_ADD(p, TR_MMA_TEMPTY);
             DBG_SET(p, DBG_MMA_WAIT, 0);
           }
@@ -927,7 +1048,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           if (!ok) break;
           if constexpr (kPair) mma_commit_pair(&tfull[acc], 0x3);
           else mma_commit(&tfull[acc]);
-          if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
+          accs.used(acc);
         }
         if constexpr (kPair) mma_commit_pair(drain, 0x1);
         else mma_commit(drain);
@@ -935,17 +1056,21 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         TRACE_FLUSH(p);
       }
       __syncwarp();
+    } else if (warp >= 6) {
+      // ---------------- ring fill spread over the GEMM CTAs
+      if (p.spread) gather_role_spread(p, cta, p.n_gemm, s_ok + 1);
     } else if (warp >= 2 && warp < 6) {
       // ---------------- epilogue
       const int q = warp & 3;
       const int row = q * 32 + lane;
-      uint32_t acc = 0, acc_phase = 0;
+      AccSeq accs;
       bool routed_done = false;
       const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
       TRACE_LOCALS();
       for (int u = walk.first; u < walk.n_units; u += walk.step) {
         const int ti = walk.task(u);
         const Task t = p.tasks[ti];
+        const uint32_t acc = accs.next(task_is_mx(p, t.kind));
         // one thread waits and decides for all four warps, so that they agree
         // on stopping and never strand each other at the named barrier
         if (threadIdx.x == 64) {
@@ -953,7 +1078,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           DBG_SET(p, DBG_EPI_TASK, ti);
           DBG_SET(p, DBG_EPI_WAIT, 1);
           TRACE_T0();
-          int ok = wait_bar(&tfull[acc], acc_phase) ? 1 : 0;
+          int ok = wait_bar(&tfull[acc], accs.uses(acc) & 1u) ? 1 : 0;
           DBG_SET(p, DBG_EPI_WAIT, 0);
           if (ok && t.kind == TASK_S2 && !routed_done)  // the combine reads every routed output row
             ok = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
@@ -1005,7 +1130,10 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows, rel);
         } else if (t.kind == TASK_R2) {
           const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
-          epilogue_copy_f16(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
+          if (p.mx)
+            epilogue_copy_f16(taddr, p.Y + y_offset(p, j / p.k, j % p.k, t.n), row < r0 + nrows, rel);
+          else
+            epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
         } else {
           epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, rel);
         }
@@ -1020,7 +1148,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           if (t.done1 >= 0) red_release_add_gpu(p.counters + t.done1, 1);
           DBG_SET(p, DBG_EPI_DONE, u);
         }
-        if (++acc == n_acc) { acc = 0; acc_phase ^= 1u; }
+        accs.used(acc);
       }
       if (threadIdx.x == 64) TRACE_FLUSH(p);
     }

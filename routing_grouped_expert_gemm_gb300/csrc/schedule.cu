@@ -366,7 +366,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           tk.need0 = tk.need1 = 0;
         } else if (!down) {
           tk.dep0 = p.direct ? -1 : ctr_filled(p, m);  // direct dispatch: x itself is the A operand
-          tk.need0 = p.G;
+          tk.need0 = p.gparts;
           tk.dep1 = m >= p.slots ? ctr_r2(p, m - p.slots) : -1;
           tk.need1 = need_h;
           tk.done0 = ctr_hready(p, mtb + i);

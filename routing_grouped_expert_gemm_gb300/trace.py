@@ -4,9 +4,9 @@
 
 Builds the MOE_TRACE variant of the library (every wait of the persistent
 kernel timed with clock64 in registers and added to per-CTA slots once, at
-the end), runs a few BF16 forwards of a seeded workload from moe_inputs and
+the end), runs a few forwards of a seeded workload from moe_inputs and
 prints, per role, the mean and maximum time per CTA spent in each kind of
-wait or epilogue, plus the mean time from a stage's TMA issue to its full
+wait or epilogue (BF16 or MXFP8 workloads), plus the mean time from a stage's TMA issue to its full
 barrier being seen by the MMA issuer.  The timed waits perturb the kernel a
 little: use it to see where time goes, not for throughput figures.
 """
@@ -21,7 +21,7 @@ os.environ["MOE_TRACE_BUILD"] = "1"
 
 NAMES = ["start", "end", "prod_dep", "prod_empty", "mma_full", "mma_tempty", "epi_tfull", "epi_busy",
          "gather_wait", "gather_busy", "final_wait", "last_task", "epi_R1", "epi_R2", "epi_S1", "epi_S2",
-         "tma_lat_ns", "tma_stages"]
+         "tma_lat_ns", "tma_stages", "g_loadwait", "g_storewait"]
 SLOTS = len(NAMES)  # the kernel's TRACE_SLOTS
 
 
@@ -41,8 +41,6 @@ def main(argv: list[str]) -> int:
     name = argv[0] if argv else "dsv3"
     cfg = json.loads(argv[1]) if len(argv) > 1 else {}
     shape = mi.CONFIGS[name]
-    if shape.precision != "bf16":
-        raise SystemExit("trace: BF16 workloads only")
     inp = mi.make_inputs(shape)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
     w = {"W_router": dev(inp.w_router),
@@ -53,7 +51,17 @@ def main(argv: list[str]) -> int:
     x = dev(inp.x)
     T = shape.T
     out = torch.empty((T, shape.D), dtype=torch.bfloat16, device="cuda")
-    plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score, **cfg)
+    plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,
+                              precision=shape.precision, **cfg)
+    if shape.precision == "mxfp8":  # routed weights as E4M3 codes + block scales
+        for nm, rows, K in (("W_up", shape.E * shape.I, shape.D), ("W_gate", shape.E * shape.I, shape.D),
+                            ("W_down", shape.E * shape.D, shape.I)):
+            q = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+            sc = torch.empty(rg.moe_mxfp8_scale_bytes(rows, K), dtype=torch.uint8, device="cuda")
+            rg.moe_quantize_mxfp8(plan, w[nm], rows, K, q, sc)
+            torch.cuda.synchronize()
+            w[nm], w[nm + "_scale"] = q, sc
+        torch.cuda.empty_cache()
     wsb = rg.moe_workspace_bytes(plan, T)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     for _ in range(4):
@@ -73,7 +81,7 @@ def main(argv: list[str]) -> int:
         if len(rows) == 0:
             continue
         print(label)
-        for i in range(2, 16):
+        for i in list(range(2, 16)) + [18, 19]:
             if i == 11:
                 continue
             v = rows[:, i] / clk

@@ -86,7 +86,7 @@ def check_mx(inp, res, rows=None, bound_unquantised=6e-2):
     return rel_mx, rel_bf
 
 
-@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+@pytest.mark.parametrize("dispatch", ["ring", "direct", "spread"])
 def test_mx_layer_small_all_tokens(dispatch):
     inp = mx_inputs(600, 512, 256, 16, 4, 256, cid=500)
     _, res = run_mx(inp, minibatch=512, ring_slots=2, gather_ctas=3, dispatch=dispatch)
@@ -111,6 +111,7 @@ def test_mx_bitwise_deterministic_across_knobs():
                dict(minibatch=128, ring_slots=3, gather_ctas=1, lag=0), dict(minibatch=4096, ring_slots=1,
                                                                               gather_ctas=8, lag=0),
                dict(minibatch=512, ring_slots=2, dispatch="direct"),
+               dict(minibatch=256, ring_slots=2, dispatch="spread"),
                dict(minibatch=128, ring_slots=1, lag=0, dispatch="direct")):
         _, res = run_mx(inp, **kw)
         outs.append(res["out"].view(torch.int16).cpu().numpy())

@@ -63,7 +63,8 @@ def test_pair_bitwise_deterministic_across_knobs():
                dict(minibatch=8192, ring_slots=1, gather_ctas=2, lag=0, gemm_ctas=20),
                dict(minibatch=512, ring_slots=5, gather_ctas=16, lag=1, gemm_ctas=6),
                dict(minibatch=1024, ring_slots=3, gather_ctas=4, raster=2),
-               dict(minibatch=256, ring_slots=2, gather_ctas=2, raster=3)):
+               dict(minibatch=256, ring_slots=2, gather_ctas=2, raster=3),
+               dict(minibatch=512, ring_slots=3, dispatch="spread")):
         layer = g.Layer(inp, mma_pair=1, **kw)
         res = layer.run(x, poison=True)
         assert res["status"] == 0

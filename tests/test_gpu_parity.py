@@ -63,18 +63,19 @@ def run_and_check(inp, T=None, **plan_kw):
     return layer, x, res
 
 
-@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+@pytest.mark.parametrize("dispatch", ["ring", "direct", "spread"])
 def test_tiny_workload_all_tokens(dispatch):
     run_and_check(mi.make_inputs("tiny"), minibatch=512, ring_slots=2, gather_ctas=2, dispatch=dispatch)
 
 
-@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+@pytest.mark.parametrize("dispatch", ["ring", "direct", "spread"])
 def test_medium_ragged_tokens_and_tiles(dispatch):
     # 1000 tokens: ragged 128-token tail, several column tiles, partial M-tiles per expert
     run_and_check(small(1000, 512, 256, 32, 6, 256), minibatch=1024, ring_slots=3, gather_ctas=4, dispatch=dispatch)
 
 
-@pytest.mark.parametrize("T,dispatch", [(1, "ring"), (127, "ring"), (129, "ring"), (1, "direct"), (129, "direct")])
+@pytest.mark.parametrize("T,dispatch", [(1, "ring"), (127, "ring"), (129, "ring"), (1, "direct"), (129, "direct"),
+                                        (1, "spread"), (129, "spread")])
 def test_edge_token_counts(T, dispatch):
     inp = small(256, 256, 128, 16, 4, 128, cid=301)
     run_and_check(inp, T=T, minibatch=128, ring_slots=2, gather_ctas=1, dispatch=dispatch)
@@ -124,6 +125,8 @@ def test_bitwise_deterministic_across_knobs():
                dict(minibatch=1024, ring_slots=3, gather_ctas=4, raster=1),
                dict(minibatch=512, ring_slots=4, gather_ctas=4, raster=3),
                dict(minibatch=1024, ring_slots=3, dispatch="direct"),
+               dict(minibatch=512, ring_slots=2, dispatch="spread"),
+               dict(minibatch=1024, ring_slots=3, dispatch="spread", gemm_ctas=9),
                dict(minibatch=128, ring_slots=1, lag=0, dispatch="direct", gemm_ctas=11)):
         layer = g.Layer(inp, **kw)
         res = layer.run(x, poison=True)
@@ -152,7 +155,7 @@ def _full_size(name, n_sample=48, **plan_kw):
     return g.check_out(got, ref)
 
 
-@pytest.mark.parametrize("dispatch", ["ring", "direct"])
+@pytest.mark.parametrize("dispatch", ["ring", "direct", "spread"])
 def test_full_size_dsv3_zipf_sampled(dispatch):
     _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8, dispatch=dispatch)
 
