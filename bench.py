@@ -59,10 +59,14 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 sub-measurement")
     ap.add_argument("--gather-ctas-mx", type=int, default=6, help="gather CTAs for the MXFP8 layer")
-    ap.add_argument("--dispatch", choices=["ring", "direct"], default="ring")
-    ap.add_argument("--mma-pair", type=int, default=0, choices=[0, 1],
-                    help="BF16 layer: CTA-pair (cta_group::2) expert tiles")
+    ap.add_argument("--dispatch", choices=["ring", "direct", "spread"], default="ring",
+                    help="BF16 layer: how the routed tokens reach the expert tiles")
+    ap.add_argument("--dispatch-mx", choices=["ring", "direct", "spread"], default="spread",
+                    help="MXFP8 layer: the same choice (spread measured fastest on DSV3)")
+    ap.add_argument("--mma-pair", type=int, default=1, choices=[0, 1],
+                    help="BF16 layer: CTA-pair (cta_group::2) expert tiles (measured fastest on DSV3)")
     ap.add_argument("--raster", type=int, default=0, help="up/gate tile order: M-tiles per group (0 = default)")
+    ap.add_argument("--gemm-ctas", type=int, default=0, help="CTAs that run expert tiles (0 = all remaining SMs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: a smaller case with this many tokens (uniform routing)")
     ap.add_argument("--experts", type=int, default=0,
@@ -227,13 +231,20 @@ def workload_config(shape, args, extra=None):
            "T": shape.T, "D": shape.D, "I": shape.I, "E": shape.E, "k": shape.k, "I_s": shape.I_s,
            "score": shape.score, "load": "Zipf(1.1) via router bias" if shape.load == "zipf" else shape.load,
            "precision": shape.precision, "minibatch": args.minibatch, "ring_slots": args.ring_slots,
-           "gather_ctas": args.gather_ctas, "lag": args.lag, "dispatch": args.dispatch,
+           "gather_ctas": (args.gather_ctas_mx if shape.precision == "mxfp8" else args.gather_ctas)
+           if dispatch_of(shape, args) == "ring" else 0,
+           "lag": args.lag, "dispatch": dispatch_of(shape, args),
            "mma_pair": args.mma_pair if shape.precision == "bf16" else 0, "raster": args.raster,
+           "gemm_ctas": args.gemm_ctas or "all remaining SMs",
            "l2": "inputs larger than L2 (expert weights 22.5 GB, x 235 MB for dsv3); no flush",
            "parallelism": "replicas"}
     if extra:
         cfg["note"] = extra
     return cfg
+
+
+def dispatch_of(shape, args) -> str:
+    return args.dispatch_mx if shape.precision == "mxfp8" else args.dispatch
 
 
 # ----------------------------------------------------------------------------- recorded DRAM traffic
@@ -268,7 +279,7 @@ def recorded_traffic(key: str, cfg: dict):
                 rec[parts[0]] = parts[1].strip()
     if rec.get("sources_sha256") != kernel_sources_hash():
         return None
-    for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch"):
+    for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch", "gemm_ctas"):
         if k in rec and str(cfg.get(k)) != rec[k]:
             return None
     try:
@@ -291,7 +302,8 @@ class Runner:
                                        ring_slots=args.ring_slots,
                                        gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8"
                                        else args.gather_ctas,
-                                       lag=args.lag, dispatch=args.dispatch, raster=args.raster,
+                                       lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
+                                       gemm_ctas=args.gemm_ctas,
                                        mma_pair=args.mma_pair if shape.precision == "bf16" else 0)
         w = {"W_router": dev(inp.w_router),
              "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()}
@@ -473,7 +485,7 @@ def run_ours(args, world, rank, local):
             "workload": "dsv3_mxfp8: DSV3 shape, uniform routing, routed experts MXFP8, shared expert BF16",
             "value": replica_throughput(world, mshape.T, args.steps, m_el), "unit": "tokens/s",
             "ms_per_step": m_el / args.steps, "tflops": world * mshape.flops() * args.steps / (m_el / 1000.0) / 1e12,
-            "gather_ctas": args.gather_ctas_mx,
+            "config": workload_config(mshape, args),
             "phases_ms_mean": {"router_topk": statistics.mean(mres["router_ms"]),
                                "schedule": statistics.mean(mres["sched_ms"]), "megakernel": m_mega},
             "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": m_ach, "peak": mx_peak,

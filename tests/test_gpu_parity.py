@@ -162,3 +162,7 @@ def test_full_size_dsv3_zipf_sampled(dispatch):
 
 def test_full_size_qwen3_sampled():
     _full_size("qwen3", minibatch=4096, ring_slots=4, gather_ctas=8, dispatch="direct")
+
+
+def test_full_size_kimi_k2_sampled_spread():
+    _full_size("kimi_k2", minibatch=8192, ring_slots=4, dispatch="spread")
