@@ -25,19 +25,20 @@ extern "C" {
 int moe_testing_mx_tile(const void* A, const void* B, const void* sf_img, float* D, int mode, void* stream);
 
 /*
- * One bf16 tcgen05.mma.cta_group::2 tile on a pair of CTAs (a cluster of 2):
- *   D [256, 256] fp32 = A [256, 64] B [256, 64]^T
- * A and B bf16 row-major (K contiguous), device pointers, 16-byte aligned.
- * CTA r of the pair loads A rows [128r, 128r+128) and B rows [128r, 128r+128)
- * with TMA into its own shared memory, both CTAs' loads counted on the even
- * CTA's mbarrier; the even CTA issues four M=256 N=256 K=16 MMAs and commits
- * to a barrier in both CTAs; CTA r writes D rows [128r, 128r+128) from its
- * TMEM.  status (device, int[3], zeroed by the caller): [0] set if the even
- * CTA's wait for the loads ran out (2 s), [1 + r] if CTA r's wait for the MMA
- * did.  Asynchronous on `stream`.  Returns 0, -1 (bad argument) or -4 (CUDA
- * error).
+ * One bf16 tcgen05.mma.cta_group::2 tile on a pair of CTAs (a cluster of 2).
+ *   m = 256: D = A [256, 64] B [256, 64]^T; CTA r loads A rows [128r, 128r+128)
+ *   m = 128: D = A [128, 64] B [256, 64]^T; CTA r loads A rows [64r, 64r+64)
+ * and B rows [128r, 128r+128), with TMA into its own shared memory, both
+ * CTAs' loads counted on the even CTA's mbarrier; the even CTA issues four
+ * M=m N=256 K=16 MMAs and commits to a barrier in both CTAs; CTA r then copies
+ * all 128 lanes x 256 columns of its TMEM to D [2][128][256] fp32 (lanes the
+ * MMA did not write hold unspecified values).  A and B bf16 row-major (K
+ * contiguous), device pointers, 16-byte aligned.  status (device, int[3],
+ * zeroed by the caller): [0] set if the even CTA's wait for the loads ran out
+ * (2 s), [1 + r] if CTA r's wait for the MMA did.  Asynchronous on `stream`.
+ * Returns 0, -1 (bad argument) or -4 (CUDA error).
  */
-int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, void* stream);
+int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, int m, void* stream);
 
 #ifdef __cplusplus
 }

@@ -97,7 +97,7 @@ def lib():
     L.moe_route_static_scratch_bytes.restype = sz
     L.moe_testing_mx_tile.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_mx_tile.restype = ctypes.c_int
-    L.moe_testing_pair_tile.argtypes = [vp, vp, vp, vp, vp]
+    L.moe_testing_pair_tile.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_pair_tile.restype = ctypes.c_int
     L.moe_error_string.argtypes = [ctypes.c_int]
     L.moe_error_string.restype = ctypes.c_char_p

@@ -5,10 +5,13 @@
 // rows of D each CTA's TMEM receives) against a CPU reference.  Not part of
 // the forward path.
 //
-// D [256, 256] fp32 = A [256, 64] B [256, 64]^T, A and B bf16 row-major (K
-// contiguous).  CTA r of the pair loads A rows [128 r, 128 r + 128) and B rows
-// [128 r, 128 r + 128); the even CTA issues four M = 256, N = 256, K = 16 MMAs;
-// CTA r then writes D rows [128 r, 128 r + 128) from its own TMEM.
+// m = 256: D [256, 256] fp32 = A [256, 64] B [256, 64]^T, A and B bf16
+// row-major (K contiguous).  CTA r of the pair loads A rows [128 r, 128 r +
+// 128) and B rows [128 r, 128 r + 128); the even CTA issues four M = 256,
+// N = 256, K = 16 MMAs.  m = 128: A [128, 64], CTA r loads A rows [64 r, 64 r
+// + 64) (and the same B halves); the MMAs are M = 128.  Either way CTA r then
+// writes all 128 TMEM lanes x 256 columns it holds to D_raw [2][128][256]
+// (lanes the MMA did not write hold whatever was there).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,10 +36,10 @@ __device__ bool probe_wait(uint64_t* bar, uint32_t parity) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     pair_probe_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, float* D,
-                      int* status) {
+                      int* status, int m) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;          // 128 rows x 128 B (64 bf16), 128-byte swizzle
+  uint8_t* sA = smem;          // 128 (m = 256) or 64 (m = 128) rows x 128 B (64 bf16), 128-byte swizzle
   uint8_t* sB = smem + 16384;  // 128 rows x 128 B
   __shared__ __align__(8) uint64_t full;
   __shared__ __align__(8) uint64_t done;
@@ -60,13 +63,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 
   if (threadIdx.x == 0) {
     const uint32_t full_even = mapa_shared(&full, rank & ~1u);
-    if ((rank & 1u) == 0) mbar_arrive_expect_tx(&full, 2u * 32768u);  // both CTAs' A and B halves
-    tma_load_2d_pair(sA, &mA, full_even, 0, (int)(128 * rank));
+    const uint32_t a_bytes = m == 256 ? 16384u : 8192u;
+    if ((rank & 1u) == 0) mbar_arrive_expect_tx(&full, 2u * (a_bytes + 16384u));  // both CTAs' A and B halves
+    tma_load_2d_pair(sA, &mA, full_even, 0, (int)((m / 2) * rank));
     tma_load_2d_pair(sB, &mB, full_even, 0, (int)(128 * rank));
     if ((rank & 1u) == 0) {
       if (probe_wait<true>(&full, 0)) {
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(256, 256);
+        const uint32_t idesc = idesc_bf16_f32((uint32_t)m, 256);
         const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
@@ -87,7 +91,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
       uint32_t r[32];
       tmem_ld_32x32b_x32(tmem + lane_base + c, r);
       tmem_ld_wait();
-      for (int j = 0; j < 32; ++j) D[(size_t)(128 * rank + row) * 256 + c + j] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j) D[((size_t)rank * 128 + row) * 256 + c + j] = __uint_as_float(r[j]);
     }
   } else if (lane == 0) {
     atomicExch(status + 1 + rank, 1);
@@ -108,10 +112,10 @@ typedef CUresult (*probe_encode_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_
                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-int encode_probe_map(probe_encode_fn enc, CUtensorMap* m, const void* ptr) {
-  cuuint64_t dims[2] = {64, 256};
+int encode_probe_map(probe_encode_fn enc, CUtensorMap* m, const void* ptr, uint32_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {64, rows};
   cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -122,8 +126,8 @@ int encode_probe_map(probe_encode_fn enc, CUtensorMap* m, const void* ptr) {
 
 }  // namespace
 
-extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, void* stream) {
-  if (!A || !B || !D || !status) return -1;
+extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, int m, void* stream) {
+  if (!A || !B || !D || !status || (m != 128 && m != 256)) return -1;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return -1;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -131,12 +135,12 @@ extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int
       q != cudaDriverEntryPointSuccess || !fn)
     return -4;
   CUtensorMap mA, mB;
-  if (encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mA, A) ||
-      encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mB, B))
+  if (encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mA, A, (uint32_t)m, (uint32_t)m / 2) ||
+      encode_probe_map(reinterpret_cast<probe_encode_fn>(fn), &mB, B, 256, 128))
     return -1;
   const int smem = 32 * 1024 + 1024;
   if (cudaFuncSetAttribute(moe::pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return -4;
-  moe::pair_probe_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(mA, mB, D, status);
+  moe::pair_probe_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(mA, mB, D, status, m);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
