@@ -40,6 +40,15 @@ int moe_testing_mx_tile(const void* A, const void* B, const void* sf_img, float*
  */
 int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, int m, void* stream);
 
+/*
+ * The same tile, with the four MMAs issued `reps` times back to back
+ * (accumulating) and the even CTA's %globaltimer span from the first issue to
+ * their completion written to *ns (device memory): the pair MMA's issue rate
+ * for M = m.  Returns 0, -1 or -4 as above.
+ */
+int moe_testing_pair_mma_time(const void* A, const void* B, float* D, int* status, int m, int reps,
+                              unsigned long long* ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,7 @@ __device__ bool probe_wait(uint64_t* bar, uint32_t parity) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
     pair_probe_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB, float* D,
-                      int* status, int m) {
+                      int* status, int m, int reps, unsigned long long* ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;          // 128 (m = 256) or 64 (m = 128) rows x 128 B (64 bf16), 128-byte swizzle
@@ -72,10 +72,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32((uint32_t)m, 256);
         const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                        kk > 0 ? 1u : 0u);
+        const uint64_t t0 = globaltimer_ns();
+        // reps > 1: the same four MMAs again, accumulating (timing only)
+        for (int rep = 0; rep < reps; ++rep)
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_pair(tmem, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                          (rep | kk) > 0 ? 1u : 0u);
         mma_commit_pair(&done, 0x3);
+        if (ns) {
+          probe_wait<true>(&done, 0);
+          *ns = globaltimer_ns() - t0;
+        }
       } else {
         atomicExch(status, 1);
       }
@@ -126,8 +133,18 @@ int encode_probe_map(probe_encode_fn enc, CUtensorMap* m, const void* ptr, uint3
 
 }  // namespace
 
+namespace moe {
+int launch_pair_probe(const void* A, const void* B, float* D, int* status, int m, int reps, unsigned long long* ns,
+                      void* stream);
+}
+
 extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, int m, void* stream) {
-  if (!A || !B || !D || !status || (m != 128 && m != 256)) return -1;
+  return moe::launch_pair_probe(A, B, D, status, m, 1, nullptr, stream);
+}
+
+int moe::launch_pair_probe(const void* A, const void* B, float* D, int* status, int m, int reps,
+                           unsigned long long* ns, void* stream) {
+  if (!A || !B || !D || !status || (m != 128 && m != 256) || reps < 1) return -1;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return -1;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -141,6 +158,14 @@ extern "C" int moe_testing_pair_tile(const void* A, const void* B, float* D, int
   const int smem = 32 * 1024 + 1024;
   if (cudaFuncSetAttribute(moe::pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return -4;
-  moe::pair_probe_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(mA, mB, D, status, m);
+  moe::pair_probe_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(mA, mB, D, status, m, reps, ns);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// Time `reps` x 4 back-to-back pair MMAs (M = m, N = 256, K = 16) on one CTA pair: *ns (device
+// memory) receives the even CTA's %globaltimer span from the first issue to the completion.
+extern "C" int moe_testing_pair_mma_time(const void* A, const void* B, float* D, int* status, int m, int reps,
+                                         unsigned long long* ns, void* stream) {
+  if (!ns) return -1;
+  return moe::launch_pair_probe(A, B, D, status, m, reps, ns, stream);
 }
