@@ -49,6 +49,21 @@ int moe_testing_pair_tile(const void* A, const void* B, float* D, int* status, i
 int moe_testing_pair_mma_time(const void* A, const void* B, float* D, int* status, int m, int reps,
                               unsigned long long* ns, void* stream);
 
+/*
+ * One block-scaled MXFP8 tcgen05.mma.cta_group::2 tile (E4M3 x E4M3, E8M0
+ * scales per 32 K-elements) on a CTA pair:
+ *   D [256, 256] fp32 = sum_{kb<4} A[:, 32kb:+32] B[:, 32kb:+32]^T * sa(row, kb) * sb(col, kb)
+ * A, B [256, 128] E4M3 codes row-major; sf = four 512-byte scale blocks (A
+ * rows 0-127, A rows 128-255, B rows 0-127, B rows 128-255) in the layout of
+ * moe_testing_mx_tile.  CTA r loads A and B rows [128r, 128r+128) and copies
+ * (tcgen05.cp.cta_group::2) its A block to TMEM column 256 and, mode 0, its
+ * own B half's block to column 260, or, mode 1, both B blocks to 260 and 264;
+ * the MMA reads A scales at 256 and B scales at 260.  D and status as for
+ * moe_testing_pair_tile.  Returns 0, -1 (bad argument) or -4 (CUDA error).
+ */
+int moe_testing_pair_mx_tile(const void* A, const void* B, const void* sf, float* D, int* status, int mode,
+                             void* stream);
+
 #ifdef __cplusplus
 }
 #endif

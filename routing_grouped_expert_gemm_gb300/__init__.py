@@ -101,6 +101,8 @@ def lib():
     L.moe_testing_pair_tile.restype = ctypes.c_int
     L.moe_testing_pair_mma_time.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp]
     L.moe_testing_pair_mma_time.restype = ctypes.c_int
+    L.moe_testing_pair_mx_tile.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
+    L.moe_testing_pair_mx_tile.restype = ctypes.c_int
     L.moe_error_string.argtypes = [ctypes.c_int]
     L.moe_error_string.restype = ctypes.c_char_p
     _lib = L

@@ -119,9 +119,11 @@ def test_mx_bitwise_deterministic_across_knobs():
         assert np.array_equal(o, outs[0])
 
 
-def test_mx_full_size_dsv3_sampled():
+@pytest.mark.parametrize("dispatch", ["direct", "spread"])
+def test_mx_full_size_dsv3_sampled(dispatch):
+    # spread: the launch configuration the benchmark times
     inp = mi.make_inputs("dsv3_mxfp8")
-    _, res = run_mx(inp, minibatch=8192, ring_slots=4, dispatch="direct")
+    _, res = run_mx(inp, minibatch=8192, ring_slots=4, dispatch=dispatch)
     s = inp.shape
     logits = oracle.router_logits(inp.x, inp.w_router, inp.b_router)
     idx_ref, g_ref = oracle.topk(logits, s.k, s.score)
