@@ -64,7 +64,7 @@ def parse_args():
     ap.add_argument("--dispatch-mx", choices=["ring", "direct", "spread"], default="spread",
                     help="MXFP8 layer: the same choice (spread measured fastest on DSV3)")
     ap.add_argument("--mma-pair", type=int, default=1, choices=[0, 1],
-                    help="BF16 layer: CTA-pair (cta_group::2) expert tiles (measured fastest on DSV3)")
+                    help="CTA-pair (cta_group::2) expert tiles, BF16 and MXFP8 (measured fastest on DSV3)")
     ap.add_argument("--raster", type=int, default=0, help="up/gate tile order: M-tiles per group (0 = default)")
     ap.add_argument("--gemm-ctas", type=int, default=0, help="CTAs that run expert tiles (0 = all remaining SMs)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -234,7 +234,7 @@ def workload_config(shape, args, extra=None):
            "gather_ctas": (args.gather_ctas_mx if shape.precision == "mxfp8" else args.gather_ctas)
            if dispatch_of(shape, args) == "ring" else 0,
            "lag": args.lag, "dispatch": dispatch_of(shape, args),
-           "mma_pair": args.mma_pair if shape.precision == "bf16" else 0, "raster": args.raster,
+           "mma_pair": args.mma_pair, "raster": args.raster,
            "gemm_ctas": args.gemm_ctas or "all remaining SMs",
            "l2": "inputs larger than L2 (expert weights 22.5 GB, x 235 MB for dsv3); no flush",
            "parallelism": "replicas"}
@@ -304,7 +304,7 @@ class Runner:
                                        else args.gather_ctas,
                                        lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
                                        gemm_ctas=args.gemm_ctas,
-                                       mma_pair=args.mma_pair if shape.precision == "bf16" else 0)
+                                       mma_pair=args.mma_pair)
         w = {"W_router": dev(inp.w_router),
              "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()}
         for name, arr, rows, K in (("W_up", inp.w_up, shape.E * shape.I, shape.D),

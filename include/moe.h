@@ -98,8 +98,11 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              two 128-row M-tiles sharing the weight tile, each CTA loading
  *              half of it (half the operand bytes per SM of the one-CTA tile);
  *              a segment with an odd number of M-tiles pads its last pair.
- *              bf16 precision with ring dispatch only (MOE_ERR_INVALID_ARG
- *              otherwise); gather_ctas must be even.  0: one CTA per tile.
+ *              With mxfp8 the scale blocks of both CTAs' rows travel with the
+ *              pair's loads and every CTA holds the weight tile's scales for
+ *              all 256 columns.  Ring or spread dispatch (direct gives
+ *              MOE_ERR_INVALID_ARG); gather_ctas must be even.  Results are
+ *              bitwise those of the one-CTA tiles.  0: one CTA per tile.
  *   raster     order of an expert segment's up/gate tiles: groups of `raster`
  *              M-tiles, each group sweeping all I/128 column tiles (so a
  *              group's token rows are re-read from L2 while its weight

@@ -16,7 +16,7 @@ cudaError_t launch_router(const RouterMaps& maps, const FwdParams& p, cudaStream
 cudaError_t launch_schedule(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream);
 int megakernel_smem_bytes();
-int megakernel_pair_max_ctas();
+int megakernel_pair_max_ctas(bool mx);
 cudaError_t launch_mx_quantize(const bf16* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st);
 size_t mx_scale_bytes(int64_t rows, int64_t K);
@@ -112,6 +112,18 @@ int encode_bf16_2d(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+// 512-byte MX scale blocks seen as rows of 128 bytes: box {128, 4} is one block
+int encode_sf_blocks(const moe_plan* pl, CUtensorMap* m, const void* ptr, size_t bytes) {
+  cuuint64_t dims[2] = {128, bytes / 128};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 4};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = pl->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -160,7 +172,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
   if (c.mma_pair) c.raster = (c.raster + 1) & ~1;  // a pair's two tasks share a column tile
   if (c.dispatch == MOE_DISPATCH_SPREAD) c.gather_ctas = 0;  // the GEMM CTAs' spare warps gather
-  if (c.mma_pair && (c.precision != MOE_PREC_BF16 || c.dispatch == MOE_DISPATCH_DIRECT || (c.gather_ctas & 1) ||
+  if (c.mma_pair && (c.dispatch == MOE_DISPATCH_DIRECT || (c.gather_ctas & 1) ||
                      (c.gemm_ctas & 1)))
     return MOE_ERR_INVALID_ARG;
   if (c.dispatch == MOE_DISPATCH_DIRECT) c.gather_ctas = 0;  // the GEMM producers gather
@@ -173,7 +185,8 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED_DEVICE;
   // CTAs resident at once: one per SM, or for CTA pairs as many as whole
   // clusters of 2 can be placed
-  const int resident = c.mma_pair ? megakernel_pair_max_ctas() : prop.multiProcessorCount;
+  const int resident =
+      c.mma_pair ? megakernel_pair_max_ctas(c.precision == MOE_PREC_MXFP8) : prop.multiProcessorCount;
   if (resident < 2) return MOE_ERR_CUDA;
   const int gemm = c.gemm_ctas > 0 ? c.gemm_ctas : resident - c.gather_ctas;
   if (gemm < (c.mma_pair ? 2 : 1) || c.gather_ctas + gemm > resident) return MOE_ERR_INVALID_ARG;
@@ -350,7 +363,14 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
     rc |= encode_u8_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);
     rc |= encode_u8_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
     rc |= encode_u8_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
-    rc |= encode_u8_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, BN_DOWN);
+    rc |= encode_u8_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, down_box);
+    if (c.mma_pair) {  // scale blocks through tensor maps (loads counted on the even CTA's barrier)
+      rc |= encode_sf_blocks(pl, &tm.sf_x, p.sfx, (size_t)L.n_mtiles_max * (c.D / BK_MX) * SF_BLOCK_BYTES);
+      rc |= encode_sf_blocks(pl, &tm.sf_h, p.sfh, (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES);
+      rc |= encode_sf_blocks(pl, &tm.sf_up, w->W_up_scale, mx_scale_bytes(c.E * c.I, c.D));
+      rc |= encode_sf_blocks(pl, &tm.sf_gate, w->W_gate_scale, mx_scale_bytes(c.E * c.I, c.D));
+      rc |= encode_sf_blocks(pl, &tm.sf_down, w->W_down_scale, mx_scale_bytes(c.E * c.D, c.I));
+    }
   } else {
     if (!p.direct) rc |= encode_bf16_2d(pl, &tm.ring_x, p.ring_x, ring_rows, c.D, BM);
     rc |= encode_bf16_2d(pl, &tm.w_up, w->W_up, c.E * c.I, c.D, BN_UP);

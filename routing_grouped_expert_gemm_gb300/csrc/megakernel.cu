@@ -679,13 +679,16 @@ __device__ void combine_role(const FwdParams& p) {
 // Stage geometry of the two kernel flavours: one CTA per tile (A 128 rows + B
 // 256 rows per stage, MXFP8 scale blocks after them) or CTA pairs (A 128 rows
 // + B 128 rows per CTA and stage).
-template <bool kPair>
+// kMx (pairs only): the routed tiles are MXFP8, whose stages also carry scale blocks.
+template <bool kPair, bool kMx = false>
 struct MegaGeom {
-  static constexpr int stages = kPair ? PAIR_STAGES : STAGES;
-  static constexpr int stride = kPair ? PAIR_STAGE_BYTES : STAGE_STRIDE;
+  static constexpr int stages = kPair ? (kMx ? PAIR_MX_STAGES : PAIR_STAGES) : STAGES;
+  static constexpr int stride = kPair ? (kMx ? PAIR_MX_STAGE_STRIDE : PAIR_STAGE_BYTES) : STAGE_STRIDE;
   static constexpr int smem_bytes = stages * stride + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
 };
-static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448, "shared memory");
+static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448 &&
+                  MegaGeom<true, true>::smem_bytes <= 232448,
+              "shared memory");
 
 template <bool kPair>
 __device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
@@ -728,9 +731,9 @@ struct TaskWalk {
   __device__ __forceinline__ int task(int u) const { return pair ? 2 * u + rank : u; }
 };
 
-template <bool kPair>
+template <bool kPair, bool kMxPair = false>
 __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParams& p) {
-  using G = MegaGeom<kPair>;
+  using G = MegaGeom<kPair, kMxPair>;
   constexpr int NST = G::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024_mk(smem_raw);
@@ -882,10 +885,29 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 #endif
           if constexpr (kPair) {
             if (lead_lane) {
-              if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)PAIR_STAGE_BYTES);
+              if (leader)
+                mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(mx ? PAIR_MX_STAGE_TX : PAIR_STAGE_BYTES));
               const uint32_t fb = full_even + stage * 8u;
               tma_load_2d_pair(sa, o.a, fb, kc, t.a_row);
               tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
+              if constexpr (kMxPair) {
+                if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
+                  uint8_t* ssf2 = sa + PAIR_STAGE_BYTES;
+                  if (t.kind == TASK_R1) {
+                    const int nkg1 = p.D / BK_MX;
+                    const int ub = (t.e * p.I + t.n * BN_UP) / BM;
+                    tma_load_2d_pair(ssf2, &maps.sf_x, fb, 0, 4 * (t.mt * nkg1 + kb));
+                    tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_up, fb, 0, 4 * (ub * nkg1 + kb));
+                    tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_gate, fb, 0, 4 * (ub * nkg1 + kb));
+                  } else {
+                    const int nkg2 = p.I / BK_MX;
+                    const int rb = (t.e * p.D + t.n * BN_DOWN) / BM;
+                    tma_load_2d_pair(ssf2, &maps.sf_h, fb, 0, 4 * (t.mt * nkg2 + kb));
+                    tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * (rb * nkg2 + kb));
+                    tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * ((rb + 1) * nkg2 + kb));
+                  }
+                }
+              }
             }
           } else {
             if (gather_a)
@@ -962,7 +984,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       if (leader && elect_one()) {
         TRACE_LOCALS();
         const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * BM : BM, 256);
-        const uint32_t idesc_mx = idesc_mxf8_e4m3(BM, 256);
+        const uint32_t idesc_mx = idesc_mxf8_e4m3(kPair ? 2 * BM : BM, 256);
         uint32_t stage = 0, phase = 0;
         AccSeq accs;
         bool ok = true;
@@ -1015,10 +1037,27 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
             const uint32_t a_addr = smem_u32(smem + stage * G::stride);
             const uint32_t b_addr = a_addr + A_STAGE_BYTES;
             if constexpr (kPair) {
+              bool mx_step = false;
+              if constexpr (kMxPair) mx_step = mx;
+              if (mx_step) {
+                if constexpr (kMxPair) {
+                  // both CTAs' scale blocks -> their TMEM, then four 32-wide K blocks
+                  const uint32_t sf = a_addr + PAIR_STAGE_BYTES;
+                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
+                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
+                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
 #pragma unroll
-              for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                mma_bf16_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
-                              (kb | kk) != 0 ? 1u : 0u);
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_mxf8_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
+                                  idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
+                                  tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                  mma_bf16_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+              }
               mma_commit_pair(&empty[stage], 0x3);
             } else {
               if (mx) {
@@ -1195,11 +1234,20 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
   mega_body<true>(maps, p);
 }
 
+// CTA pairs with MXFP8 routed tiles
+__global__ void __launch_bounds__(MEGA_THREADS, 1)
+    moe_megakernel_pair_mx(const __grid_constant__ TensorMaps maps, const FwdParams p) {
+  mega_body<true, true>(maps, p);
+}
+
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream) {
-  const bool pair = p.pair != 0;
-  const void* fn = pair ? reinterpret_cast<const void*>(moe_megakernel_pair)
-                        : reinterpret_cast<const void*>(moe_megakernel);
-  const int smem = pair ? MegaGeom<true>::smem_bytes : MegaGeom<false>::smem_bytes;
+  const bool pair = p.pair != 0, pair_mx = pair && p.mx;
+  const void* fn = pair_mx ? reinterpret_cast<const void*>(moe_megakernel_pair_mx)
+                   : pair  ? reinterpret_cast<const void*>(moe_megakernel_pair)
+                           : reinterpret_cast<const void*>(moe_megakernel);
+  const int smem = pair_mx ? MegaGeom<true, true>::smem_bytes
+                   : pair  ? MegaGeom<true>::smem_bytes
+                           : MegaGeom<false>::smem_bytes;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -1216,6 +1264,7 @@ cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int gr
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pair ? 2 : 1;
+  if (pair_mx) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair_mx, maps, p);
   if (pair) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair, maps, p);
   return cudaLaunchKernelEx(&cfg, moe_megakernel, maps, p);
 }
@@ -1223,10 +1272,11 @@ cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int gr
 int megakernel_smem_bytes() { return MegaGeom<false>::smem_bytes; }
 
 // CTAs of the pair kernel that can be resident at once (clusters of 2, one CTA per SM)
-int megakernel_pair_max_ctas() {
-  const int smem = MegaGeom<true>::smem_bytes;
-  if (cudaFuncSetAttribute(moe_megakernel_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return -1;
+int megakernel_pair_max_ctas(bool mx) {
+  const int smem = mx ? MegaGeom<true, true>::smem_bytes : MegaGeom<true>::smem_bytes;
+  const void* fn = mx ? reinterpret_cast<const void*>(moe_megakernel_pair_mx)
+                      : reinterpret_cast<const void*>(moe_megakernel_pair);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return -1;
@@ -1242,7 +1292,7 @@ int megakernel_pair_max_ctas() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, moe_megakernel_pair, &cfg) != cudaSuccess) return -1;
+  if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) return -1;
   return 2 * clusters;
 }
 

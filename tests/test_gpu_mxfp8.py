@@ -131,3 +131,51 @@ def test_mx_full_size_dsv3_sampled(dispatch):
     compare_routing(res, idx_ref, g_ref, s.E)
     rows = np.unique(np.linspace(0, s.T - 1, 32).astype(np.int64))
     check_mx(inp, res, rows=rows)
+
+
+# CTA pairs (mma_pair = 1): one block-scaled tcgen05.mma.cta_group::2 per
+# expert tile over two 128-row M-tiles; each CTA's scale blocks come in with
+# the pair's tensor-map loads and the even CTA copies them into both CTAs'
+# TMEM.  Same bars as the one-CTA kernel.
+@pytest.mark.parametrize("dispatch", ["ring", "spread"])
+def test_mx_pair_layer_small_all_tokens(dispatch):
+    inp = mx_inputs(600, 512, 256, 16, 4, 256, cid=510)
+    _, res = run_mx(inp, minibatch=512, ring_slots=2, gather_ctas=2, dispatch=dispatch, mma_pair=1)
+    check_mx(inp, res)
+
+
+@pytest.mark.parametrize("T", [1, 129, 333])
+def test_mx_pair_ragged_no_shared(T):
+    # T = 1: every expert tile is one token plus an empty partner
+    import gpu_util
+    inp = mx_inputs(333, 256, 128, 8, 3, 0, cid=511)
+    layer = gpu_util.Layer(inp, minibatch=256, ring_slots=2, gather_ctas=2, mma_pair=1)
+    res = layer.run(gpu_util.to_dev_bf16(inp.x[:T]), T, poison=True)
+    assert res["status"] == 0
+    check_mx(inp, res, rows=np.arange(T), bound_unquantised=1e-1)
+
+
+def test_mx_pair_bitwise_deterministic_across_knobs():
+    inp = mx_inputs(700, 512, 256, 16, 4, 256, cid=512)
+    outs = []
+    for kw in (dict(minibatch=512, ring_slots=2, gather_ctas=2), dict(minibatch=512, ring_slots=2, gather_ctas=2),
+               dict(minibatch=128, ring_slots=3, gather_ctas=2, lag=0),
+               dict(minibatch=4096, ring_slots=1, gather_ctas=8, lag=0, gemm_ctas=10),
+               dict(minibatch=256, ring_slots=2, dispatch="spread"),
+               dict(minibatch=512, ring_slots=3, dispatch="spread", raster=2)):
+        _, res = run_mx(inp, mma_pair=1, **kw)
+        outs.append((kw, res["out"].view(torch.int16).cpu().numpy()))
+    for kw, o in outs[1:]:
+        assert np.array_equal(o, outs[0][1]), f"output bits differ for {kw}"
+
+
+def test_mx_pair_full_size_dsv3_sampled():
+    inp = mi.make_inputs("dsv3_mxfp8")
+    _, res = run_mx(inp, minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)
+    s = inp.shape
+    logits = oracle.router_logits(inp.x, inp.w_router, inp.b_router)
+    idx_ref, g_ref = oracle.topk(logits, s.k, s.score)
+    from test_gpu_parity import compare_routing
+    compare_routing(res, idx_ref, g_ref, s.E)
+    rows = np.unique(np.linspace(0, s.T - 1, 32).astype(np.int64))
+    check_mx(inp, res, rows=rows)

@@ -75,7 +75,7 @@ def test_pair_bitwise_deterministic_across_knobs():
 
 def test_pair_rejects_unsupported_modes():
     import routing_grouped_expert_gemm_gb300 as rg
-    for kw in (dict(precision="mxfp8"), dict(dispatch="direct"), dict(gather_ctas=3)):
+    for kw in (dict(precision="mxfp8", dispatch="direct"), dict(dispatch="direct"), dict(gather_ctas=3)):
         with pytest.raises(rg.MoEError):
             rg.moe_plan_create(256, 256, 128, 16, 4, 128, mma_pair=1, **kw)
 
