@@ -37,14 +37,13 @@ static_assert(STAGE_BYTES + SF_STAGE_BYTES <= STAGE_STRIDE && STAGE_STRIDE % 102
 constexpr int PAIR_B_STAGE_BYTES = 128 * BK * 2;  // 16 KB
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + PAIR_B_STAGE_BYTES;  // 32 KB per CTA
 constexpr int PAIR_STAGES = 6;
-// CTA pairs, MXFP8 routed tiles: per CTA and stage its A codes, its half of
-// B's codes, the A scale block of its rows and B's two scale blocks (each CTA
-// needs the scales of all 256 B rows)
+// CTA pairs, MXFP8 routed tiles: per CTA and stage its A codes and its half
+// of B's codes in the 32 KB stage, and in a separate array of 1.5 KB slots
+// (one per stage, after the stages) the A scale block of its rows and B's two
+// scale blocks (each CTA needs the scales of all 256 B rows).  Keeping the
+// scales out of the 1024-aligned stages leaves room for six stages.
 constexpr int PAIR_MX_STAGE_TX = PAIR_STAGE_BYTES + SF_STAGE_BYTES;  // 33.5 KB
-constexpr int PAIR_MX_STAGE_STRIDE = 34816;                           // 1024-aligned pitch
-constexpr int PAIR_MX_STAGES = 5;
-static_assert(PAIR_MX_STAGE_TX <= PAIR_MX_STAGE_STRIDE && PAIR_MX_STAGE_STRIDE % 1024 == 0, "pair MX stage pitch");
-constexpr int SF_TMEM_COL = 256;                  // MXFP8: scale columns after the single accumulator
+constexpr int PAIR_MX_STAGES = 6;
 constexpr int ACC_COLS = 256;    // fp32 accumulator columns per tile
 constexpr int MEGA_THREADS = 256;  // 8 warps
 constexpr int ROUTER_THREADS = 192;

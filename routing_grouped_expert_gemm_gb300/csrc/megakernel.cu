@@ -349,20 +349,27 @@ __device__ __forceinline__ void mx_scale_sources(const FwdParams& p, const Task&
 // Handing an accumulator buffer back to the MMA issuer after its last TMEM
 // read: every epilogue thread arrives on the local barrier (one CTA per tile),
 // or one lane per warp arrives on the even CTA's barrier (CTA pairs).
+// An epilogue hands its accumulator buffer back twice: the first columns once
+// they are read (an MXFP8 tile in the other buffer puts its block scales
+// there), the whole buffer after the last read.
 struct AccRelease {
   uint64_t* local;
   uint32_t remote;  // cluster address of the even CTA's barrier
+  uint64_t* head_local;
+  uint32_t head_remote;
   bool pair;
 };
-__device__ __forceinline__ void release_acc(const AccRelease& r) {
+__device__ __forceinline__ void release_bar(uint64_t* local, uint32_t remote, bool pair) {
   tc_fence_before();
-  if (r.pair) {
+  if (pair) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(r.remote);
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(remote);
   } else {
-    mbar_arrive(r.local);
+    mbar_arrive(local);
   }
 }
+__device__ __forceinline__ void release_acc(const AccRelease& r) { release_bar(r.local, r.remote, r.pair); }
+__device__ __forceinline__ void release_head(const AccRelease& r) { release_bar(r.head_local, r.head_remote, r.pair); }
 
 // 128 threads, thread r owns tile row r (TMEM lane r).
 __device__ __forceinline__ void store_row_bf16x32(bf16* dst, const float* v) {
@@ -428,6 +435,7 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, u);
     tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + c), g);
     tmem_ld_wait();
+    if (c == 0) release_head(rel);
     if (c + 32 == BN_UP) {  // last TMEM read of this tile: hand the accumulator back
       release_acc(rel);
     }
@@ -458,6 +466,7 @@ __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf
     tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), u);
     tmem_ld_32x32b_x32(taddr + (uint32_t)(BN_UP + 32 * c), g);
     tmem_ld_wait();
+    if (c == 0) release_head(rel);
     if (c == 3) {
       release_acc(rel);
     }
@@ -490,6 +499,7 @@ __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
+    if (c == 0) release_head(rel);
     if (c + 32 == BN_DOWN) release_acc(rel);
     float v[32];
 #pragma unroll
@@ -505,29 +515,6 @@ __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y
       }
     }
     __syncwarp();
-  }
-}
-
-// The same with the buffer held as briefly as possible (single-buffered
-// MXFP8 tiles): thread r owns TMEM lane r = tile row r, whose 256
-// outputs form one contiguous 512-byte staging segment at y_row: every 16
-// columns read from TMEM go straight out as one full 32-byte sector, and the
-// buffer is handed back right after the last read.
-__device__ void epilogue_copy_f16(uint32_t taddr, __half* y_row, bool valid, const AccRelease& rel) {
-#pragma unroll
-  for (int c = 0; c < BN_DOWN; c += 16) {
-    uint32_t r[16];
-    tmem_ld_32x32b_x16(taddr + (uint32_t)c, r);
-    tmem_ld_wait();
-    if (c + 16 == BN_DOWN) release_acc(rel);
-    uint32_t h[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = pack_f16x2_sat(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-    if (valid) {
-      uint4* d = reinterpret_cast<uint4*>(y_row + c);
-      d[0] = make_uint4(h[0], h[1], h[2], h[3]);
-      d[1] = make_uint4(h[4], h[5], h[6], h[7]);
-    }
   }
 }
 
@@ -645,6 +632,7 @@ __device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdP
       uint32_t r[32];
       tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
       tmem_ld_wait();
+      if (c == 0) release_head(rel);
       if (c + 32 == BN_DOWN) {
         release_acc(rel);
       }
@@ -679,12 +667,14 @@ __device__ void combine_role(const FwdParams& p) {
 // Stage geometry of the two kernel flavours: one CTA per tile (A 128 rows + B
 // 256 rows per stage, MXFP8 scale blocks after them) or CTA pairs (A 128 rows
 // + B 128 rows per CTA and stage).
-// kMx (pairs only): the routed tiles are MXFP8, whose stages also carry scale blocks.
+// kMx (pairs only): the routed tiles are MXFP8; their scale blocks take one
+// slot per stage after the stages.
 template <bool kPair, bool kMx = false>
 struct MegaGeom {
   static constexpr int stages = kPair ? (kMx ? PAIR_MX_STAGES : PAIR_STAGES) : STAGES;
-  static constexpr int stride = kPair ? (kMx ? PAIR_MX_STAGE_STRIDE : PAIR_STAGE_BYTES) : STAGE_STRIDE;
-  static constexpr int smem_bytes = stages * stride + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+  static constexpr int stride = kPair ? PAIR_STAGE_BYTES : STAGE_STRIDE;
+  static constexpr int sf_bytes = kMx ? stages * SF_STAGE_BYTES : 0;
+  static constexpr int smem_bytes = stages * stride + sf_bytes + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
 };
 static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448 &&
                   MegaGeom<true, true>::smem_bytes <= 232448,
@@ -701,18 +691,17 @@ __device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
   }
 }
 
-// Accumulator buffer of each task.  The two TMEM buffers alternate, except
-// that routed MXFP8 tasks always take buffer 0: their block scales sit in the
-// first columns of buffer 1.  Shared-expert tasks (which come before and after
-// every routed task) alternate in MXFP8 layers too.  Per-buffer use counts
-// give the mbarrier parities; the MMA issuer and the epilogue walk the same
-// tasks, so they pick the same buffers.
+// Accumulator buffer of each task: the two TMEM buffers alternate.  A routed
+// MXFP8 task puts its block scales in the first 12 columns of the other
+// buffer, which the previous task's epilogue hands back after its first TMEM
+// read.  Per-buffer use counts give the mbarrier parities; the MMA issuer and
+// the epilogue walk the same tasks, so they pick the same buffers.
 struct AccSeq {
   uint32_t uses0 = 0u, uses1 = 0u;  // scalars, not an array: no local memory
   uint32_t alt = 0u;
-  __device__ __forceinline__ uint32_t next(bool mx_task) {
-    const uint32_t b = mx_task ? 0u : alt;
-    if (!mx_task) alt ^= 1u;
+  __device__ __forceinline__ uint32_t next() {
+    const uint32_t b = alt;
+    alt ^= 1u;
     return b;
   }
   __device__ __forceinline__ uint32_t uses(uint32_t b) const { return b ? uses1 : uses0; }
@@ -737,16 +726,18 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   constexpr int NST = G::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024_mk(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * G::stride);
+  uint8_t* sf_slots = smem + NST * G::stride;  // pairs with MXFP8 tiles: scale blocks per stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_slots + G::sf_bytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + NST;
   uint64_t* tfull = bars + 2 * NST;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* thead = tempty + 2;  // first columns of a buffer read by its epilogue
+  uint64_t* drain = thead + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = s_flag + 1;
-  EpiStage* epi = reinterpret_cast<EpiStage*>(smem + NST * G::stride + 256);
+  EpiStage* epi = reinterpret_cast<EpiStage*>(sf_slots + G::sf_bytes + 256);
 #ifdef MOE_TRACE
   volatile uint64_t* s_issue_ns = bars + 24;  // per stage: when its loads were issued (trace builds)
 #endif
@@ -780,6 +771,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       for (int a = 0; a < 2; ++a) {
         mbar_init(&tfull[a], 1);
         mbar_init(&tempty[a], kPair ? 8 : 128);  // pairs: one arrival per epilogue warp of both CTAs
+        mbar_init(&thead[a], kPair ? 8 : 128);
       }
       mbar_init(drain, 1);
       fence_barrier_init();
@@ -892,7 +884,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
               if constexpr (kMxPair) {
                 if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
-                  uint8_t* ssf2 = sa + PAIR_STAGE_BYTES;
+                  uint8_t* ssf2 = sf_slots + stage * SF_STAGE_BYTES;
                   if (t.kind == TASK_R1) {
                     const int nkg1 = p.D / BK_MX;
                     const int ub = (t.e * p.I + t.n * BN_UP) / BM;
@@ -995,7 +987,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           const int kind = p.tasks[walk.task(u)].kind;
           const bool mx = task_is_mx(p, kind);
           const int nk = task_nk(p, kind);
-          const uint32_t acc = accs.next(mx);
+          const uint32_t acc = accs.next();
           DBG_SET(p, DBG_MMA_UNIT, u);
           DBG_SET(p, DBG_MMA_ACC, acc);
 #ifdef MOE_DEBUG_LOG
@@ -1014,13 +1006,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
             DBG_SET(p, DBG_MMA_WAIT, 1);
             TRACE_T0();
             if (!wait_bar(&tempty[acc], (accs.uses(acc) & 1u) ^ 1u)) break;
-            // MXFP8: the block scales go to buffer 1's first columns, which its last user must have released
-            if (mx && accs.uses1 > 0 && !wait_bar(&tempty[1], (accs.uses1 & 1u) ^ 1u)) break;
+            // MXFP8: the block scales go to the other buffer's first columns, which its latest user must have read
+            const uint32_t o = acc ^ 1u;
+            if (mx && accs.uses(o) > 0 && !wait_bar(&thead[o], (accs.uses(o) & 1u) ^ 1u)) break;
             TRACE_ADD(p, TR_MMA_TEMPTY);
             DBG_SET(p, DBG_MMA_WAIT, 0);
           }
           tc_fence_after();
           const uint32_t d = tmem + acc * ACC_COLS;
+          const uint32_t sfc = tmem + (acc ^ 1u) * ACC_COLS;  // MXFP8 scale columns: A, B rows 0-127, B rows 128-255
           for (int kb = 0; kb < nk; ++kb) {
             {
               DBG_SET(p, DBG_MMA_WAIT, 2);
@@ -1042,15 +1036,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               if (mx_step) {
                 if constexpr (kMxPair) {
                   // both CTAs' scale blocks -> their TMEM, then four 32-wide K blocks
-                  const uint32_t sf = a_addr + PAIR_STAGE_BYTES;
-                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
-                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
-                  tmem_cp_32x128b_warpx4_pair(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
+                  const uint32_t sf = smem_u32(sf_slots) + stage * SF_STAGE_BYTES;
+                  tmem_cp_32x128b_warpx4_pair(sfc, sdesc_sf_block(sf));
+                  tmem_cp_32x128b_warpx4_pair(sfc + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
+                  tmem_cp_32x128b_warpx4_pair(sfc + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)
                     mma_mxf8_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
-                                  idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
-                                  tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
+                                  idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sfc, sfc + 4,
+                                  (kb | kk) != 0 ? 1u : 0u);
                 }
               } else {
 #pragma unroll
@@ -1063,14 +1057,14 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               if (mx) {
                 // scales -> TMEM (in order with the MMAs below), then four 32-wide K blocks
                 const uint32_t sf = a_addr + STAGE_BYTES;
-                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL, sdesc_sf_block(sf));
-                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
-                tmem_cp_32x128b_warpx4(tmem + SF_TMEM_COL + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
+                tmem_cp_32x128b_warpx4(sfc, sdesc_sf_block(sf));
+                tmem_cp_32x128b_warpx4(sfc + 4, sdesc_sf_block(sf + SF_BLOCK_BYTES));
+                tmem_cp_32x128b_warpx4(sfc + 8, sdesc_sf_block(sf + 2 * SF_BLOCK_BYTES));
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   mma_mxf8_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32),
-                              idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), tmem + SF_TMEM_COL,
-                              tmem + SF_TMEM_COL + 4, (kb | kk) != 0 ? 1u : 0u);
+                              idesc_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sfc, sfc + 4,
+                              (kb | kk) != 0 ? 1u : 0u);
               } else {
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
@@ -1105,11 +1099,12 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       AccSeq accs;
       bool routed_done = false;
       const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
+      const uint32_t thead_even = kPair ? mapa_shared(thead, 0) : 0u;
       TRACE_LOCALS();
       for (int u = walk.first; u < walk.n_units; u += walk.step) {
         const int ti = walk.task(u);
         const Task t = p.tasks[ti];
-        const uint32_t acc = accs.next(task_is_mx(p, t.kind));
+        const uint32_t acc = accs.next();
         // one thread waits and decides for all four warps, so that they agree
         // on stopping and never strand each other at the named barrier
         if (threadIdx.x == 64) {
@@ -1159,7 +1154,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         }
 #endif
         EpiStage& st = epi[q];
-        const AccRelease rel{&tempty[acc], tempty_even + acc * 8u, kPair};
+        const AccRelease rel{&tempty[acc], tempty_even + acc * 8u, &thead[acc], thead_even + acc * 8u, kPair};
         if (t.kind == TASK_R1 && p.mx) {
           epilogue_swiglu_mx(taddr, reinterpret_cast<uint8_t*>(p.ring_h) + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
                              p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows, rel);
@@ -1169,10 +1164,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           epilogue_swiglu(taddr, st, p.h_s + (size_t)(t.out_row + r0) * p.I_s + t.n * BN_UP, p.I_s, nrows, rel);
         } else if (t.kind == TASK_R2) {
           const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
-          if (p.mx)
-            epilogue_copy_f16(taddr, p.Y + y_offset(p, j / p.k, j % p.k, t.n), row < r0 + nrows, rel);
-          else
-            epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
+          epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
         } else {
           epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, rel);
         }
