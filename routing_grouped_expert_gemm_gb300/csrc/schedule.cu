@@ -182,6 +182,11 @@ __device__ __forceinline__ void piece_rows(const int* sS, int e, int m, int b, i
   z = min(sS[e + 1], (m + 1) * b);
 }
 
+// A operand row of an empty partner task: the whole 128-row box lies before
+// the tensor, so TMA fills it with zeros without reading memory (and the
+// tensor cores multiply zeros, which draws less power than real rows).
+constexpr int NO_ROWS = -BM;
+
 __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   __shared__ int s_seg[E_MAX];  // per expert: segment count, then first segment
   __shared__ int s_mt[E_MAX];   // per expert: M-tile count, then first M-tile
@@ -301,12 +306,12 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
     const int mt = p.pair ? 2 * (qq / (2 * nn)) + (qq & 1) : qq / nn;
     const int n = p.pair ? (qq >> 1) % nn : qq % nn;
     const bool real = mt < p.n_smtiles;
-    const int mtr = real ? mt : mt - 1;  // an empty partner reads its partner's rows
+    const int mtr = real ? mt : mt - 1;  // an empty partner takes its partner's rows (A: none)
     Task tk;
     tk.kind = down ? TASK_S2 : TASK_S1;
     tk.n = n;
     tk.e = 0;
-    tk.a_row = mtr * BM;
+    tk.a_row = real ? mtr * BM : NO_ROWS;
     tk.rows = real ? min(BM, p.T - mt * BM) : 0;
     tk.p0 = mtr * BM;
     tk.out_row = mtr * BM;
@@ -351,16 +356,16 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           n = within / gc;
         }
         const bool real = i < cnt;
-        const int ir = real ? i : i - 1;  // an empty partner reads its partner's rows
+        const int ir = real ? i : i - 1;  // an empty partner takes its partner's rows (A: none)
         const int r0 = a + ir * BM;
         Task tk;
         tk.kind = down ? TASK_R2 : TASK_R1;
         tk.n = n;
         tk.e = e;
-        tk.a_row = slot_row + (r0 - m * b);
+        tk.out_row = slot_row + (r0 - m * b);
+        tk.a_row = real ? tk.out_row : NO_ROWS;
         tk.rows = real ? min(BM, z - r0) : 0;
         tk.p0 = r0;
-        tk.out_row = tk.a_row;
         if (!real) {
           tk.dep0 = tk.dep1 = tk.done0 = tk.done1 = -1;
           tk.need0 = tk.need1 = 0;
