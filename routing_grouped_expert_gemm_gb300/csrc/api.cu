@@ -80,7 +80,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.xs = take(mx ? (size_t)T * (c.D / 32) : 0);
   L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
-  L.Y = take((size_t)L.n_chunks * BM * c.k * c.D * 2);  // blocked by token tile, see FwdParams::Y
+  L.Y = take((size_t)L.n_chunks * BM * (c.k + (c.I_s > 0 ? 1 : 0)) * c.D * 2);  // blocked by token tile, see FwdParams::Y
 #ifdef MOE_TRACE
   L.trace = take(sizeof(unsigned long long) * TRACE_SLOTS * 1024);
 #endif
@@ -276,6 +276,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.I = (int)c.I;
   p.E = (int)c.E;
   p.k = (int)c.k;
+  p.kY = (int)c.k + (shared ? 1 : 0);  // a call without the shared weights has no slot k
   p.I_s = shared ? (int)c.I_s : 0;
   p.score_fn = c.score_fn;
   p.mx = mx ? 1 : 0;

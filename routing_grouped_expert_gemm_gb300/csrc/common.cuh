@@ -74,12 +74,13 @@ struct __align__(16) Task {  // 64 bytes
 static_assert(sizeof(Task) == 64, "task record is 64 bytes");
 
 // meta block written by the schedule kernel (int32 offsets)
-enum : int { META_N_TASKS = 0, META_N_MTILES = 1, META_TOTAL_Y = 2 /* R2 tasks */, META_MB = 4 };
+enum : int { META_N_TASKS = 0, META_N_MTILES = 1, META_TOTAL_Y = 2 /* real R2 and S2 tasks */, META_MB = 4 };
 // per minibatch m, META_MB + 4 m + {0: R1 task count, 1: R2 task count,
 // 2: first M-tile, 3: M-tile count}
 
 struct FwdParams {
   int T, D, I, E, k, I_s;
+  int kY;               // staging slots per token: k routed, plus 1 for the shared expert's output
   int score_fn;
   int mx;               // routed experts in MXFP8 (1) or BF16 (0)
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
@@ -123,9 +124,10 @@ struct FwdParams {
   const uint8_t* w_gate_sf;
   const uint8_t* w_down_sf;
   bf16* h_s;          // [T, I_s]
-  __half* Y;          // fp16 staging rows of the routed outputs, blocked: for token tile tt = t / 128 and
-                      // column tile n (256 columns), block (tt, n) holds [128 tokens][k slots][256 columns]
-                      // contiguously, so one shared-expert down tile's combine reads one 128 k 512-byte block
+  __half* Y;          // fp16 staging rows of the expert outputs, blocked: for token tile tt = t / 128 and
+                      // column tile n (256 columns), block (tt, n) holds [128 tokens][kY slots][256 columns]
+                      // contiguously (slots 0..k-1 routed, slot k the shared expert), so the combine reads
+                      // one kY x 512-byte block per token and column tile
   bf16* out;          // [T, D]
   unsigned long long* trace;  // [grid, TRACE_SLOTS] when built with MOE_TRACE, else null
   int* dbg;           // MOE_DEBUG_LOG builds: [grid, DBG_SLOTS] progress records in host memory, else null
@@ -138,7 +140,9 @@ enum : int {
   TR_GATHER_WAIT, TR_GATHER_BUSY, TR_FINAL_WAIT, TR_TASKS, TR_EPI_R1, TR_EPI_R2, TR_EPI_S1, TR_EPI_S2,
   TR_TMA_LAT_NS /* stage issue -> full barrier seen by the MMA issuer, summed */, TR_TMA_STAGES,
   TR_GATHER_LOADWAIT /* bulk gather: waiting for a row load */, TR_GATHER_STOREWAIT /* ... for stores to drain */,
-  TRACE_SLOTS = 20
+  TR_START_CLK /* clock64 at TR_START_NS */, TR_END_CLK /* ... at TR_END_NS: the SM clock over the run */,
+  TR_COMBINE /* the final combine pass */,
+  TRACE_SLOTS = 23
 };
 // Each thread that times anything keeps its sums in registers (TRACE_LOCALS)
 // and adds them to the CTA's slots once, at the end (TRACE_FLUSH), so the
@@ -211,7 +215,7 @@ __host__ __device__ inline int ctr_shready(const FwdParams& p, int mt) {
 }
 // the 256 staging columns of column tile n for route (token t, slot s)
 __host__ __device__ inline size_t y_offset(const FwdParams& p, int t, int s, int n) {
-  return ((((size_t)(t / BM) * p.N2 + n) * BM + (size_t)(t % BM)) * p.k + s) * BN_DOWN;
+  return ((((size_t)(t / BM) * p.N2 + n) * BM + (size_t)(t % BM)) * p.kY + s) * BN_DOWN;
 }
 __host__ __device__ inline int n_counters(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
 

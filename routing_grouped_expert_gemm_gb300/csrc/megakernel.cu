@@ -15,12 +15,14 @@
 //    the host and no token is dropped.
 //  * Sec. 3.4 "Shared Expert": the shared expert's up/gate tiles come first,
 //    while the first minibatch is being gathered; its down-projection tiles
-//    come last and carry the weighted sum in their epilogue (the shared
-//    output never leaves TMEM in fp32 before it is added).
+//    come last and store the shared output as one more staging slot per
+//    token.
 //  * Sec. 3.4 "Determinism": no floating-point atomics; every output element
 //    is produced by one tile with a fixed K order, and the weighted sum runs
 //    in a fixed slot order from a token-order fp16 staging buffer (10
-//    mantissa bits: the sum's error stays below the bf16 output rounding).
+//    mantissa bits: the sum's error stays below the bf16 output rounding),
+//    once every staging row is stored, on all CTAs at once (a pass bound by
+//    HBM bandwidth, with many loads in flight per warp).
 // The expert FFN is the one of Sec. 2.1 / the blog's E_i(x) with SiLU:
 // h = SiLU(x W_gate^T) * (x W_up^T) in fp32 from TMEM, stored bf16; y = h W_down^T.
 //
@@ -43,7 +45,7 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: two accumulator buffers
 constexpr int GATHER_BUFS = 32;          // row buffers of a gather CTA (at most)
 constexpr int GATHER_STORES = 4;         // row stores a gather CTA keeps in flight
 constexpr int GATHER_TOK_CHUNK = 4096;   // rows whose tokens a gather CTA stages in shared memory at a time
-constexpr int EPI_STAGE_BYTES = 4 * 6272;  // 4 epilogue warps x sizeof(EpiStage)
+constexpr int EPI_STAGE_BYTES = 4 * 4224;  // 4 epilogue warps x sizeof(EpiStage)
 
 // ------------------------------------------------------------------ MXFP8 helpers
 // byte offset of (row r of a 128-row block, K-block kb of a 128-wide K step)
@@ -363,7 +365,7 @@ __device__ __forceinline__ void release_bar(uint64_t* local, uint32_t remote, bo
   tc_fence_before();
   if (pair) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(remote);
+    if ((threadIdx.x & 31) == 0) mbar_arrive_remote(remote);
   } else {
     mbar_arrive(local);
   }
@@ -392,9 +394,8 @@ __device__ __forceinline__ void store_row_bf16x32(bf16* dst, const float* v) {
 // every warp store then covers 4 rows x a contiguous 32-column segment.
 struct EpiStage {
   float v[32][33];
-  float g[32][TOPK_MAX];  // router weights of the warp's 32 tokens (combine)
 };
-static_assert(sizeof(EpiStage) == 6272, "epilogue staging size");
+static_assert(sizeof(EpiStage) == 4224, "epilogue staging size");
 
 __device__ __forceinline__ void stage_block(EpiStage& st, const float* v) {
   const int lane = threadIdx.x & 31;
@@ -519,40 +520,19 @@ __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y
 }
 
 // ------------------------------------------------------------------ combine
-// Weighted sum back in token order (Eq. MoE), fp32, slot order 0..k-1, one
-// rounding to bf16 at the end.  With a shared expert the sum is fused into the
-// shared expert's down-projection epilogue and starts from its fp32 output;
-// without one, this pass runs once every routed output row is stored.
-__device__ __forceinline__ void accumulate_routed(const FwdParams& p, int t, int col, const float* g, float* acc) {
-  const __half* y = p.Y + y_offset(p, t, 0, col / BN_DOWN) + col % BN_DOWN;
-#pragma unroll
-  for (int s = 0; s < TOPK_MAX; ++s) {
-    if (s < p.k) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 f = load_f16x4(y + (size_t)s * BN_DOWN + 4 * i);
-        acc[4 * i + 0] = fmaf(g[s], f.x, acc[4 * i + 0]);
-        acc[4 * i + 1] = fmaf(g[s], f.y, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(g[s], f.z, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(g[s], f.w, acc[4 * i + 3]);
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void load_g(const FwdParams& p, int t, bool valid, float* g) {
-#pragma unroll
-  for (int s = 0; s < TOPK_MAX; ++s) g[s] = (valid && s < p.k) ? p.topk_w[(size_t)t * p.k + s] : 0.0f;
-}
-
-// shared-expert down projection + combine: out = bf16(y_s + sum_slot g * Y[t k + slot]),
-// y_s in fp32 straight from TMEM; t0 = token of the warp's first row.
-// The staging rows are the combine's only large read (k D fp16 per token):
-// lane l handles rows 8i + l/4 and 8 columns (16 bytes) at 8 (l % 4) of each
-// 32-column chunk, and a chunk's 4 rows x 8 slots of loads are all issued
-// before the first is used, so that enough bytes are in flight to cover
-// the memory latency (the tile was prefetched into L2 by the producer).
-constexpr int CMB_SLOTS = 8;  // slots per batch of loads
+// Weighted sum back in token order (Eq. MoE), in fp32 with one rounding to
+// bf16 at the end: out[t] = y_s[t] + g[t,0] Y[t,0] + ... + g[t,k-1] Y[t,k-1],
+// the shared expert's output (staging slot k; absent without a shared expert)
+// first, then the routed slots in slot order, whatever order the tiles ran in.
+// It runs on every CTA once every staging row is stored, as a stream bound by
+// HBM bandwidth.  A unit is one token and one 256-column tile; its kY staging
+// rows are one contiguous block of kY x 512 bytes, and units in staging order
+// are consecutive blocks.  A round is 8 consecutive units, one per warp; each
+// CTA takes a contiguous range of rounds and streams them into its (idle)
+// stage buffers with one bulk copy per round, up to CMB_BUFS rounds ahead;
+// lane l of a warp sums columns 8l .. 8l + 7 of its unit from shared memory.
+constexpr int CMB_BUFS = 8;
+constexpr int CMB_BAR_OFFSET = 1024;  // barriers in the epilogue staging area, past the gather's
 
 __device__ __forceinline__ void fma_f16x8(float* acc, float g, uint4 w) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -564,103 +544,82 @@ __device__ __forceinline__ void fma_f16x8(float* acc, float g, uint4 w) {
   }
 }
 
-__device__ void epilogue_shared_combine(uint32_t taddr, EpiStage& st, const FwdParams& p, int t0, int col0,
-                                        int nrows, const AccRelease& rel) {
-  const int lane = threadIdx.x & 31;
-  const int k = p.k;
-#pragma unroll
-  for (int s = 0; s < TOPK_MAX; ++s) st.g[lane][s] = (lane < nrows && s < k) ? p.topk_w[(size_t)(t0 + lane) * k + s] : 0.0f;
-  const int cc = 8 * (lane & 3);
-  __syncwarp();  // g visible to the warp
-  // rows 8i + lane/4 of a half h: i = 2h, 2h + 1
-  auto load_half = [&](uint4 (&yv)[2][CMB_SLOTS], int c, int h, int s0) {
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-      const int rr = 8 * (2 * h + ii) + (lane >> 2);
-      const __half* y = p.Y + y_offset(p, t0 + rr, s0, col0 / BN_DOWN) + c + cc;
-#pragma unroll
-      for (int s = 0; s < CMB_SLOTS; ++s)
-        yv[ii][s] = (rr < nrows && s0 + s < k) ? *reinterpret_cast<const uint4*>(y + (size_t)s * BN_DOWN)
-                                               : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  auto fma_half = [&](float (&acc)[2][8], const uint4 (&yv)[2][CMB_SLOTS], int h, int s0) {
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-      const int rr = 8 * (2 * h + ii) + (lane >> 2);
-#pragma unroll
-      for (int s = 0; s < CMB_SLOTS; ++s)
-        if (s0 + s < k) fma_f16x8(acc[ii], st.g[rr][s0 + s], yv[ii][s]);
-    }
-  };
-  auto finish_half = [&](const uint4 (&yv0)[2][CMB_SLOTS], int c, int h) {
-    float acc[2][8];
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-      const int rr = 8 * (2 * h + ii) + (lane >> 2);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[ii][j] = st.v[rr][cc + j];  // the shared expert's fp32 output
-    }
-    fma_half(acc, yv0, h, 0);
-#pragma unroll 1
-    for (int s0 = CMB_SLOTS; s0 < k; s0 += CMB_SLOTS) {  // k > 8: further slot batches
-      uint4 yv[2][CMB_SLOTS];
-      load_half(yv, c, h, s0);
-      fma_half(acc, yv, h, s0);
-    }
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-      const int rr = 8 * (2 * h + ii) + (lane >> 2);
-      if (rr < nrows) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[ii][0], acc[ii][1]);
-        o.y = pack_bf16x2(acc[ii][2], acc[ii][3]);
-        o.z = pack_bf16x2(acc[ii][4], acc[ii][5]);
-        o.w = pack_bf16x2(acc[ii][6], acc[ii][7]);
-        *reinterpret_cast<uint4*>(p.out + (size_t)(t0 + rr) * p.D + col0 + c + cc) = o;
-      }
-    }
-  };
-#pragma unroll 1
-  for (int c = 0; c < BN_DOWN; c += 32) {
-    // staging-row loads of the first half go out before the TMEM read and
-    // those of the second half before the first half is summed, so that the
-    // latencies overlap
-    uint4 ya[2][CMB_SLOTS], yb[2][CMB_SLOTS];
-    load_half(ya, c, 0, 0);
-    {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
-      tmem_ld_wait();
-      if (c == 0) release_head(rel);
-      if (c + 32 == BN_DOWN) {
-        release_acc(rel);
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) st.v[lane][j] = __uint_as_float(r[j]);
-      __syncwarp();
-    }
-    load_half(yb, c, 1, 0);
-    finish_half(ya, c, 0);
-    finish_half(yb, c, 1);
-    __syncwarp();
+// buf: buf_bytes of shared memory free for the pass; bars: CMB_BUFS free
+// mbarrier slots; ok: a shared flag.  Every thread of the CTA calls it.
+__device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, uint64_t* bars, volatile int* ok) {
+  const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  const int warps = (int)(blockDim.x >> 5);  // units per round
+  const int k = p.k, kY = p.kY;
+  const bool shared = kY > k;
+  const uint32_t unit_bytes = (uint32_t)kY * BN_DOWN * 2;
+  const uint32_t round_bytes = (uint32_t)warps * unit_bytes;
+  const int nb = min(CMB_BUFS, buf_bytes / (int)round_bytes);  // >= 2: kY <= 17 and >= 192 KB of buffers
+  const long long per_tt = (long long)p.N2 * BM;              // units of one token tile
+  const long long n_units = (long long)((p.T + BM - 1) / BM) * per_tt;
+  const long long n_rounds = (n_units + warps - 1) / warps;
+  const long long per_cta = (n_rounds + gridDim.x - 1) / gridDim.x;
+  const long long r0 = (long long)blockIdx.x * per_cta;
+  const int nr = (int)max(0ll, min(n_rounds, r0 + per_cta) - r0);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nb; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
   }
-}
-
-// no shared expert: every CTA takes tokens blockIdx.x, blockIdx.x + gridDim.x, ...
-__device__ void combine_role(const FwdParams& p) {
-  const int chunks = p.D / 32;
-  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
-    float g[TOPK_MAX];
-    load_g(p, t, true, g);
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-      float acc[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
-      accumulate_routed(p, t, c * 32, g, acc);
-      store_row_bf16x32(p.out + (size_t)t * p.D + c * 32, acc);
+  __syncthreads();
+  auto issue = [&](int i) {  // this CTA's round i into buffer i % nb
+    const long long u = (r0 + i) * warps;
+    const uint32_t bytes = (uint32_t)min((long long)warps, n_units - u) * unit_bytes;
+    mbar_arrive_expect_tx(&bars[i % nb], bytes);
+    bulk_load(buf + (size_t)(i % nb) * round_bytes, p.Y + (size_t)u * kY * BN_DOWN, bytes, &bars[i % nb]);
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(nb, nr); ++i) issue(i);
+  int issued = min(nb, nr);  // thread 0: rounds whose copies were issued
+  // router weights of the warp's next unit, loaded a round ahead: lane s holds slot s
+  auto unit_tok = [&](int i) {
+    const long long u = (r0 + i) * warps + warp;
+    const int t = (int)(u / per_tt) * BM + (int)(u % BM);
+    return (i < nr && u < n_units && t < p.T) ? t : -1;
+  };
+  int tok = unit_tok(0);
+  float g = tok >= 0 && lane < k ? p.topk_w[(size_t)tok * k + lane] : 0.0f;
+  int i = 0;
+  for (; i < nr; ++i) {
+    if (threadIdx.x == 0) *ok = mbar_wait(&bars[i % nb], (uint32_t)(i / nb) & 1u, p.status, p.timeout_ns) ? 1 : 0;
+    __syncthreads();  // also: every warp is done with round i - 1
+    if (*ok == 0) break;
+    if (threadIdx.x == 0 && i >= 1 && i - 1 + nb < nr) {  // refill the buffer round i - 1 used
+      fence_proxy_async_smem();
+      issue(i - 1 + nb);
+      ++issued;
     }
+    const int tok_next = unit_tok(i + 1);
+    const float g_next = tok_next >= 0 && lane < k ? p.topk_w[(size_t)tok_next * k + lane] : 0.0f;
+    if (tok >= 0) {
+      const __half* y = reinterpret_cast<const __half*>(buf + (size_t)(i % nb) * round_bytes +
+                                                        (size_t)warp * unit_bytes) + 8 * lane;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      if (shared) fma_f16x8(acc, 1.0f, *reinterpret_cast<const uint4*>(y + (size_t)k * BN_DOWN));  // exact
+#pragma unroll 4
+      for (int s = 0; s < k; ++s)
+        fma_f16x8(acc, __shfl_sync(0xffffffffu, g, s), *reinterpret_cast<const uint4*>(y + (size_t)s * BN_DOWN));
+      const long long u = (r0 + i) * warps + warp;
+      const int n = (int)((u / BM) % p.N2);
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.out + (size_t)tok * p.D + n * BN_DOWN + 8 * lane) = o;
+    }  // (tok is the same for the whole warp: all lanes or none take part in the shuffles)
+    tok = tok_next;
+    g = g_next;
   }
+  // copies still in flight (an abort) land before the CTA leaves
+  if (threadIdx.x == 0)
+    for (int j = i; j < issued; ++j) mbar_wait_drain(&bars[j % nb], (uint32_t)(j / nb) & 1u, p.timeout_ns);
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -744,9 +703,11 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
-  if (threadIdx.x == 0) TRACE_SET(p, TR_START_NS, globaltimer_ns());
+  if (threadIdx.x == 0) {
+    TRACE_SET(p, TR_START_NS, globaltimer_ns());
+    TRACE_SET(p, TR_START_CLK, clock64());
+  }
   if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 1);
-  const bool has_shared = p.N1s > 0;
 
   if (is_gather) {
     // the stage buffers hold rows in flight; the barriers live in the (unused) epilogue staging area
@@ -1097,7 +1058,6 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       const int q = warp & 3;
       const int row = q * 32 + lane;
       AccSeq accs;
-      bool routed_done = false;
       const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
       const uint32_t thead_even = kPair ? mapa_shared(thead, 0) : 0u;
       TRACE_LOCALS();
@@ -1112,28 +1072,14 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           DBG_SET(p, DBG_EPI_TASK, ti);
           DBG_SET(p, DBG_EPI_WAIT, 1);
           TRACE_T0();
-          int ok = wait_bar(&tfull[acc], accs.uses(acc) & 1u) ? 1 : 0;
+          const int ok = wait_bar(&tfull[acc], accs.uses(acc) & 1u) ? 1 : 0;
           DBG_SET(p, DBG_EPI_WAIT, 0);
-          if (ok && t.kind == TASK_S2 && !routed_done)  // the combine reads every routed output row
-            ok = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
-          routed_done = routed_done || (ok && t.kind == TASK_S2);
           *s_ok = ok;
           TRACE_ADD(p, TR_EPI_TFULL);
         }
         named_bar_sync(1, 128);
         if (*s_ok == 0) break;
         TRACE_T0();
-        if (threadIdx.x == 64 && u + walk.step < walk.n_units) {
-          // the next task's combine reads k staging rows per token once: bring
-          // them into L2 one epilogue ahead (a hint only; lines written later
-          // by other CTAs are updated in L2)
-          const Task nt = p.tasks[walk.task(u + walk.step)];
-          if (nt.kind == TASK_S2) {  // one contiguous block: rows x k x 256 fp16
-            const uint8_t* y0 = reinterpret_cast<const uint8_t*>(p.Y + y_offset(p, nt.out_row, 0, nt.n));
-            const uint32_t bytes = (uint32_t)nt.rows * p.k * BN_DOWN * 2;
-            for (uint32_t o = 0; o < bytes; o += 65536u) bulk_prefetch_l2(y0 + o, min(65536u, bytes - o));
-          }
-        }
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
         const int r0 = q * 32;                        // the warp's first tile row
@@ -1147,7 +1093,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           else {
             const int jj = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
             rows_ok = t.p0 + t.rows <= p.R && jj >= 0 && jj < p.R &&
-                      y_offset(p, jj / p.k, jj % p.k, t.n) + BN_DOWN <= (size_t)p.n_chunks * BM * p.k * p.D;
+                      y_offset(p, jj / p.k, jj % p.k, t.n) + BN_DOWN <= (size_t)p.n_chunks * BM * p.kY * p.D;
           }
           if (!DBG_CHECK(p, col_ok, 20, tmem, acc, ti) || !DBG_CHECK(p, rows_ok, 21 + t.kind, t.out_row, r0, ti))
             nrows = 0;
@@ -1165,8 +1111,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         } else if (t.kind == TASK_R2) {
           const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
           epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n), nrows, rel);
-        } else {
-          epilogue_shared_combine(taddr, st, p, t.out_row + r0, t.n * BN_DOWN, nrows, rel);
+        } else {  // the shared expert's output: staging slot k of its tokens
+          epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, t.out_row + row, p.k, t.n), nrows, rel);
         }
         // h tiles are read back by TMA (async proxy); Y and out only by plain loads
         if (t.kind == TASK_R1 || t.kind == TASK_S1) fence_proxy_async_global();
@@ -1198,20 +1144,30 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
     }
   }
 
-  // ---------------- combine without a shared expert: every CTA, once all routed rows are stored
-  if (!has_shared) {
-    if (threadIdx.x == 0) {
-      TRACE_LOCALS();
-      TRACE_T0();
-      *s_flag = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
-      TRACE_ADD(p, TR_FINAL_WAIT);
-      TRACE_FLUSH(p);
-    }
-    __syncthreads();
-    if (*s_flag) combine_role(p);
+  // ---------------- combine: every CTA, once every staging row is stored
+  if (threadIdx.x == 0) {
+    TRACE_LOCALS();
+    TRACE_T0();
+    *s_flag = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
+    TRACE_ADD(p, TR_FINAL_WAIT);
+    TRACE_FLUSH(p);
   }
   __syncthreads();
-  if (threadIdx.x == 0) TRACE_SET(p, TR_END_NS, globaltimer_ns());
+  if (*s_flag) {
+#ifdef MOE_TRACE
+    const long long c0 = clock64();
+#endif
+    combine_role(p, smem, NST * G::stride,
+                 reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi) + CMB_BAR_OFFSET), s_ok);
+#ifdef MOE_TRACE
+    if (threadIdx.x == 0 && p.trace) p.trace[(size_t)blockIdx.x * TRACE_SLOTS + TR_COMBINE] = clock64() - c0;
+#endif
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    TRACE_SET(p, TR_END_NS, globaltimer_ns());
+    TRACE_SET(p, TR_END_CLK, clock64());
+  }
   if (threadIdx.x == 0) DBG_SET(p, DBG_PHASE, 5);
 }
 

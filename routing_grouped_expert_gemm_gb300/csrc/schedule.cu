@@ -119,12 +119,13 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
 // Order of execution:
 //   S1 (shared expert up/gate, all tokens) ;
 //   for step s = 0 .. n_mb - 1 + lag:  R1(s) if s < n_mb ;  R2(s - lag) if s >= lag ;
-//   S2 (shared expert down projection + combine, all tokens)
+//   S2 (shared expert down projection into staging slot k, all tokens)
+// and then, in every CTA once all staging rows are stored, the combine.
 // R1(m) / R2(m): for each segment of minibatch m (an expert's rows inside m),
 // for each column tile n, for each M-tile of the segment -- the M-tiles that
 // share a weight slice run side by side (slice read from HBM once).
 // S1 / S2: token-tile major -- the column tiles of one token tile run side by
-// side, so the combine in S2 reads whole staging rows at once.
+// side.
 // A GEMM CTA takes tasks g, g + n_gemm, g + 2 n_gemm, ...; every dependency of
 // a task points to an earlier task (or to the gather, whose own dependencies
 // are earlier tasks), so the smallest unfinished task can always proceed.
@@ -290,6 +291,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
       p.meta[META_N_MTILES] = nmt_tot;
       int y = 0;
       for (int m = 0; m < n_mb; ++m) y += mb_tiles[m] * p.N2;
+      y += p.n_smtiles * p.N2s;
       p.meta[META_TOTAL_Y] = ok ? y : 0;
     }
     s_tot[0] = ok ? 1 : 0;
@@ -320,7 +322,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
     tk.dep1 = -1;
     tk.need1 = 0;
     tk.done0 = !down && real ? ctr_shready(p, mt) : -1;
-    tk.done1 = -1;
+    tk.done1 = down && real ? ctr_ydone() : -1;  // the shared output is staging slot k
     tk.mt = mtr;
     tk.pad[0] = tk.pad[1] = 0;
     store_task(p.tasks + (down ? (int)total - n_s2 + qq : qq), tk);

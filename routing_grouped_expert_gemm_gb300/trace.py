@@ -6,8 +6,9 @@ Builds the MOE_TRACE variant of the library (every wait of the persistent
 kernel timed with clock64 in registers and added to per-CTA slots once, at
 the end), runs a few forwards of a seeded workload from moe_inputs and
 prints, per role, the mean and maximum time per CTA spent in each kind of
-wait or epilogue (BF16 or MXFP8 workloads), plus the mean time from a stage's TMA issue to its full
-barrier being seen by the MMA issuer.  The timed waits perturb the kernel a
+wait or epilogue (BF16 or MXFP8 workloads; clock64 cycles converted at the SM
+clock measured over the run), plus the mean time from a stage's TMA issue to
+its full barrier being seen by the MMA issuer.  The timed waits perturb the kernel a
 little: use it to see where time goes, not for throughput figures.
 """
 from __future__ import annotations
@@ -21,7 +22,7 @@ os.environ["MOE_TRACE_BUILD"] = "1"
 
 NAMES = ["start", "end", "prod_dep", "prod_empty", "mma_full", "mma_tempty", "epi_tfull", "epi_busy",
          "gather_wait", "gather_busy", "final_wait", "last_task", "epi_R1", "epi_R2", "epi_S1", "epi_S2",
-         "tma_lat_ns", "tma_stages", "g_loadwait", "g_storewait"]
+         "tma_lat_ns", "tma_stages", "g_loadwait", "g_storewait", "start_clk", "end_clk", "combine"]
 SLOTS = len(NAMES)  # the kernel's TRACE_SLOTS
 
 
@@ -74,14 +75,15 @@ def main(argv: list[str]) -> int:
     tr = tr[tr[:, 0] != 0]  # CTAs that ran
     start = tr[:, 0].min()
     dur_us = (tr[:, 1] - start) / 1e3
-    clk = 1.95e3  # clock64 cycles per us: the SM clock this kernel runs at under load (~1.95 GHz)
-    print("kernel span us: max %.0f  min %.0f" % (dur_us.max(), dur_us.min()))
+    # clock64 cycles per us over each CTA's run: the SM clock it actually ran at
+    clk = float(np.median((tr[:, 21] - tr[:, 20]) / np.maximum(tr[:, 1] - tr[:, 0], 1) * 1e3))
+    print("kernel span us: max %.0f  min %.0f   SM clock %.0f MHz" % (dur_us.max(), dur_us.min(), clk))
     G = cfg.get("gather_ctas", 8) if cfg.get("dispatch", "ring") == "ring" else 0
     for label, rows in (("gather", tr[:G]), ("gemm", tr[G:])):
         if len(rows) == 0:
             continue
         print(label)
-        for i in list(range(2, 16)) + [18, 19]:
+        for i in list(range(2, 16)) + [18, 19, 22]:
             if i == 11:
                 continue
             v = rows[:, i] / clk
