@@ -49,7 +49,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   const int64_t pad_seg = c.mma_pair ? L.max_segs : 0, pad_sh = c.mma_pair ? 1 : 0;
   L.n_tasks_max = (L.n_mtiles_max + pad_seg) * (c.I / BN_UP + c.D / BN_DOWN) +
                   (c.I_s > 0 ? (L.n_smtiles + pad_sh) * (c.I_s / BN_UP + c.D / BN_DOWN) : 0);
-  L.n_counters = 1 + 3 * L.n_mb + L.n_mtiles_max + L.n_smtiles;
+  L.n_counters = 2 + 3 * L.n_mb + L.n_mtiles_max + L.n_smtiles;  // see ctr_claim
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;

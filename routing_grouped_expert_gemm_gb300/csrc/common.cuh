@@ -217,7 +217,9 @@ __host__ __device__ inline int ctr_shready(const FwdParams& p, int mt) {
 __host__ __device__ inline size_t y_offset(const FwdParams& p, int t, int s, int n) {
   return ((((size_t)(t / BM) * p.N2 + n) * BM + (size_t)(t % BM)) * p.kY + s) * BN_DOWN;
 }
-__host__ __device__ inline int n_counters(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
+// the GEMM CTAs' unit claims (persistent kernel)
+__host__ __device__ inline int ctr_claim(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
+__host__ __device__ inline int n_counters(const FwdParams& p) { return 2 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
 
 struct TensorMaps {
   CUtensorMap x;        // [T, D]            box {64, 128}

@@ -627,13 +627,16 @@ __device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, ui
 // 256 rows per stage, MXFP8 scale blocks after them) or CTA pairs (A 128 rows
 // + B 128 rows per CTA and stage).
 // kMx (pairs only): the routed tiles are MXFP8; their scale blocks take one
-// slot per stage after the stages.
+// slot per stage after the stages.  Then the barriers and small shared
+// variables (BAR_BYTES) and the epilogue staging.
+constexpr int BAR_BYTES = 512;
+constexpr int QN = 8;  // unit queue slots (the producer runs at most a few units ahead)
 template <bool kPair, bool kMx = false>
 struct MegaGeom {
   static constexpr int stages = kPair ? (kMx ? PAIR_MX_STAGES : PAIR_STAGES) : STAGES;
   static constexpr int stride = kPair ? PAIR_STAGE_BYTES : STAGE_STRIDE;
   static constexpr int sf_bytes = kMx ? stages * SF_STAGE_BYTES : 0;
-  static constexpr int smem_bytes = stages * stride + sf_bytes + 1024 /*align*/ + 256 /*barriers*/ + EPI_STAGE_BYTES;
+  static constexpr int smem_bytes = stages * stride + sf_bytes + 1024 /*align*/ + BAR_BYTES + EPI_STAGE_BYTES;
 };
 static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448 &&
                   MegaGeom<true, true>::smem_bytes <= 232448,
@@ -670,11 +673,16 @@ struct AccSeq {
   }
 };
 
-// Task walk: a GEMM CTA takes units first, first + step, ...; a unit is one
-// task, or with CTA pairs two consecutive tasks (2u: even CTA, 2u + 1: odd CTA)
-// that share one weight tile.
+// Units of work: a unit is one task, or with CTA pairs two consecutive tasks
+// (2u: even CTA, 2u + 1: odd CTA) that share one weight tile.  The producer of
+// each GEMM CTA (of the even CTA of a pair) claims units from a global counter
+// in increasing order, one ahead of the unit it is loading, and hands each to
+// the MMA issuer, the epilogue and (pairs) the odd CTA through a queue of QN
+// slots in shared memory.  Every dependency of a unit points to an earlier
+// unit, and every unit below the highest claimed one has been claimed, so the
+// smallest unfinished unit can always proceed.
 struct TaskWalk {
-  int first, step, n_units, rank;
+  int n_units, rank;
   bool pair;
   __device__ __forceinline__ int task(int u) const { return pair ? 2 * u + rank : u; }
 };
@@ -687,6 +695,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   uint8_t* smem = align_1024_mk(smem_raw);
   uint8_t* sf_slots = smem + NST * G::stride;  // pairs with MXFP8 tiles: scale blocks per stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf_slots + G::sf_bytes);
+  static_assert(2 * 6 + 7 <= 24 && 48 * 8 + QN * 4 <= BAR_BYTES, "barrier area");
   uint64_t* full = bars;
   uint64_t* empty = bars + NST;
   uint64_t* tfull = bars + 2 * NST;
@@ -695,8 +704,11 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   uint64_t* drain = thead + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* s_ok = s_flag + 1;
-  EpiStage* epi = reinterpret_cast<EpiStage*>(sf_slots + G::sf_bytes + 256);
+  volatile int* s_ok = s_flag + 1;  // s_ok + 1: the spread ring fill's flag, s_ok + 2: the epilogue's unit
+  uint64_t* qfull = bars + 32;       // unit queue: slot written
+  uint64_t* qempty = bars + 40;      // ... slot read by every reader
+  volatile int* qslot = reinterpret_cast<volatile int*>(bars + 48);
+  EpiStage* epi = reinterpret_cast<EpiStage*>(sf_slots + G::sf_bytes + BAR_BYTES);
 #ifdef MOE_TRACE
   volatile uint64_t* s_issue_ns = bars + 24;  // per stage: when its loads were issued (trace builds)
 #endif
@@ -720,8 +732,6 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
     TaskWalk walk;
     walk.pair = kPair;
     walk.rank = kPair ? (int)(cluster_ctarank() & 1u) : 0;
-    walk.first = kPair ? cta >> 1 : cta;
-    walk.step = kPair ? p.n_gemm >> 1 : p.n_gemm;
     walk.n_units = kPair ? n_tasks >> 1 : n_tasks;
     const bool leader = walk.rank == 0;  // the CTA that issues the MMAs
     if (threadIdx.x == 0) {
@@ -735,6 +745,10 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         mbar_init(&thead[a], kPair ? 8 : 128);
       }
       mbar_init(drain, 1);
+      for (int i = 0; i < QN; ++i) {
+        mbar_init(&qfull[i], 1);
+        mbar_init(&qempty[i], kPair ? 4 : 2);  // MMA issuer + epilogue (pairs: + the odd CTA's producer and epilogue)
+      }
       fence_barrier_init();
     }
     if (warp == 1) tmem_alloc_all<kPair>(tmem_slot);
@@ -771,10 +785,40 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       }
       // pairs: every load of both CTAs is counted on the even CTA's full barrier
       const uint32_t full_even = kPair ? mapa_shared(full, 0) : 0u;
+      const uint32_t q_odd = kPair ? mapa_shared(const_cast<int*>(qslot), 1) : 0u;
+      const uint32_t qfull_odd = kPair ? mapa_shared(qfull, 1) : 0u;
+      const uint32_t qempty_even = kPair ? mapa_shared(qempty, 0) : 0u;
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = walk.first; u < walk.n_units && ok; u += walk.step) {
+      int claim = 0;  // even / only CTA: the unit claimed for the next queue slot
+      if (lead_lane && leader) claim = atomicAdd(p.counters + ctr_claim(p), 1);
+      for (int i = 0; ok; ++i) {
+        const int slot = i % QN;
+        const uint32_t qpar = (uint32_t)(i / QN) & 1u;
+        int u = -2;  // -2: a wait ran out; -1: no units left
+        if (lead_lane) {
+          if (leader) {  // publish the claimed unit, then claim the one after it
+            if (wait_bar(&qempty[slot], qpar ^ 1u)) {
+              u = claim < walk.n_units ? claim : -1;
+              qslot[slot] = u;
+              if constexpr (kPair) {
+                st_shared_cluster_u32(q_odd + 4u * slot, (uint32_t)u);
+                mbar_arrive_remote_cluster(qfull_odd + 8u * slot);
+              }
+              mbar_arrive(&qfull[slot]);
+              if (u >= 0) claim = atomicAdd(p.counters + ctr_claim(p), 1);
+            }
+          } else if (wait_bar(&qfull[slot], qpar)) {  // odd CTA: the even CTA's unit
+            u = qslot[slot];
+          }
+        }
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (kPair && lead_lane && !leader && u != -2) mbar_arrive_remote(qempty_even + 8u * slot);
+        if (u < 0) {
+          ok = u == -1;
+          break;
+        }
         if (!DBG_CHECK(p, walk.task(u) < p.n_tasks_max, 1, u, walk.task(u), p.n_tasks_max)) break;
         const Task t = p.tasks[walk.task(u)];
         int good = 1;
@@ -944,7 +988,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 #ifdef MOE_DEBUG_LOG
         int mma_stages = 0;
 #endif
-        for (int u = walk.first; u < walk.n_units && ok; u += walk.step) {
+        for (int i = 0; ok; ++i) {
+          const int slot = i % QN;
+          if (!wait_bar(&qfull[slot], (uint32_t)(i / QN) & 1u)) break;
+          const int u = qslot[slot];
+          if (u < 0) {  // (the branch has the value: the slot may be reused after the arrive)
+            mbar_arrive(&qempty[slot]);
+            break;
+          }
+          mbar_arrive(&qempty[slot]);
           const int kind = p.tasks[walk.task(u)].kind;
           const bool mx = task_is_mx(p, kind);
           const int nk = task_nk(p, kind);
@@ -1061,12 +1113,27 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
       const uint32_t thead_even = kPair ? mapa_shared(thead, 0) : 0u;
       TRACE_LOCALS();
-      for (int u = walk.first; u < walk.n_units; u += walk.step) {
+      const uint32_t qempty_even = kPair ? mapa_shared(qempty, 0) : 0u;
+      volatile int* s_unit = s_ok + 2;
+      for (int i = 0;; ++i) {
+        // one thread waits and decides for all four warps, so that they agree
+        // on stopping and never strand each other at the named barrier
+        if (threadIdx.x == 64) {
+          const int slot = i % QN;
+          if (wait_bar(&qfull[slot], (uint32_t)(i / QN) & 1u)) {
+            *s_unit = qslot[slot];  // (the store has the value before the arrive)
+            if (kPair && !leader) mbar_arrive_remote(qempty_even + 8u * slot);
+            else mbar_arrive(&qempty[slot]);
+          } else {
+            *s_unit = -2;
+          }
+        }
+        named_bar_sync(1, 128);
+        const int u = *s_unit;
+        if (u < 0) break;
         const int ti = walk.task(u);
         const Task t = p.tasks[ti];
         const uint32_t acc = accs.next();
-        // one thread waits and decides for all four warps, so that they agree
-        // on stopping and never strand each other at the named barrier
         if (threadIdx.x == 64) {
           DBG_SET(p, DBG_EPI_UNIT, u);
           DBG_SET(p, DBG_EPI_TASK, ti);

@@ -176,6 +176,15 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// A 32-bit store into the shared memory of a CTA of the cluster
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Arrive on a barrier of another CTA of the cluster, ordering this thread's
+// earlier stores (e.g. into that CTA's shared memory) before it at cluster scope
+__device__ __forceinline__ void mbar_arrive_remote_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // Arrive on a barrier of another CTA of the cluster with release at CTA scope.
 // For an accumulator hand-back that is all that is needed: the TMEM reads
 // being released have completed (tcgen05.wait::ld, then

@@ -126,9 +126,10 @@ __global__ void __launch_bounds__(SCHED_THREADS, 1) schedule_kernel(const FwdPar
 // share a weight slice run side by side (slice read from HBM once).
 // S1 / S2: token-tile major -- the column tiles of one token tile run side by
 // side.
-// A GEMM CTA takes tasks g, g + n_gemm, g + 2 n_gemm, ...; every dependency of
-// a task points to an earlier task (or to the gather, whose own dependencies
-// are earlier tasks), so the smallest unfinished task can always proceed.
+// The GEMM CTAs claim tasks (pairs of tasks with CTA pairs) in increasing
+// order from a global counter; every dependency of a task points to an earlier
+// task (or to the gather, whose own dependencies are earlier tasks), so the
+// smallest unfinished task can always proceed.
 //
 // Segments sorted by first row are in expert-major order and every
 // minibatch's segments are contiguous, so the whole layout comes from
