@@ -380,19 +380,23 @@ class Runner:
     def e2e(self, steps, pipelined=True):
         """pinned host x -> device, forward, device -> pinned host out, every step.
 
-        pipelined: the copies run on a second stream with two device input and
-        output buffers, so that step i + 1's input copy and step i's output
-        copy overlap the forwards around them (each step still moves its own
-        input and result); otherwise copy, forward and copy run in sequence."""
+        pipelined: input copies, forwards and output copies run on three
+        streams with two device input and output buffers, so that step i + 1's
+        input copy and step i - 1's output copy overlap step i's forward (each
+        step still moves its own input and result); otherwise copy, forward
+        and copy run in sequence."""
         torch = self.torch
         x_host = torch.from_numpy(np.ascontiguousarray(self.inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
         outs_host = [torch.empty((self.shape.T, self.shape.D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         x_in = [torch.empty_like(self.x) for _ in range(2)]
         outs = [self.out, torch.empty_like(self.out)]
-        # both streams are created here: work on torch's legacy default stream
-        # would serialise with every other stream and nothing would overlap
+        # the streams are created here: work on torch's legacy default stream
+        # would serialise with every other stream; and one stream for both
+        # copy directions would queue step i + 1's input copy behind step i's
+        # output copy, which waits for step i's forward
         comp = torch.cuda.Stream() if pipelined else self.stream
         cs = torch.cuda.Stream() if pipelined else self.stream
+        cs_out = torch.cuda.Stream() if pipelined else self.stream
         Ev = torch.cuda.Event
 
         def run(n):
@@ -413,20 +417,20 @@ class Runner:
                 done = Ev()
                 done.record(comp)
                 in_free[b] = done
-                with torch.cuda.stream(cs):
-                    cs.wait_event(done)
+                with torch.cuda.stream(cs_out):
+                    cs_out.wait_event(done)
                     outs_host[b].copy_(outs[b], non_blocking=True)
                     copied = Ev()
-                    copied.record(cs)
+                    copied.record(cs_out)
                 out_free[b] = copied
 
         run(3)
         self.barrier()
         torch.cuda.synchronize()
         s0, s1 = Ev(enable_timing=True), Ev(enable_timing=True)
-        s0.record(cs)
+        s0.record(cs)  # before the first input copy
         run(steps)
-        s1.record(cs)  # after the last output copy, which followed the last forward
+        s1.record(cs_out)  # after the last output copy, which followed the last forward
         torch.cuda.synchronize()
         self.barrier()
         return {"ms": s0.elapsed_time(s1), "h2d": x_host.numel() * 2, "d2h": outs_host[0].numel() * 2}
@@ -499,7 +503,8 @@ def run_ours(args, world, rank, local):
         # "serial": copy in, forward, copy out one after the other
         line["e2e"] = {"value": replica_throughput(world, T, args.steps, e2e["ms"]), "unit": "tokens/s",
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                       "copies": "pipelined on a second stream (two device input/output buffers)",
+                       "copies": "pipelined: input copies, forwards, output copies on three streams, "
+                                 "two device input/output buffers",
                        "serial_value": replica_throughput(world, T, args.steps, e2e_serial["ms"])}
     cpu = None
     if world == 1 and not args.no_cpu_baseline and rank == 0:

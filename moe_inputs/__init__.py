@@ -91,7 +91,18 @@ CONFIGS: dict[str, MoEShape] = {
     "dsv3_mxfp8": MoEShape("dsv3_mxfp8", 16384, 7168, 2048, 256, 8, 2048, "sigmoid", "uniform",
                            precision="mxfp8", config_id=3),
     "kimi_k2": MoEShape("kimi_k2", 32768, 7168, 2048, 384, 8, 2048, "sigmoid", "uniform", config_id=4),
+    # The pages' four evaluated layer shapes (one shared expert each; its width
+    # is not given, read as I), 16384 tokens on one GPU, uniform routing; the
+    # _mxfp8 twins draw the same inputs (same config_id) with MXFP8 routed experts.
+    "kimi_k27": MoEShape("kimi_k27", 16384, 7168, 2048, 384, 8, 2048, "sigmoid", "uniform", config_id=5),
+    "glm52": MoEShape("glm52", 16384, 6144, 2048, 256, 8, 2048, "sigmoid", "uniform", config_id=6),
+    "qwen35": MoEShape("qwen35", 16384, 4096, 1024, 512, 10, 1024, "sigmoid", "uniform", config_id=7),
+    "dsv4pro": MoEShape("dsv4pro", 16384, 7168, 3072, 384, 6, 3072, "sigmoid", "uniform", config_id=8),
 }
+for _n in ("kimi_k27", "glm52", "qwen35", "dsv4pro"):
+    _b = CONFIGS[_n]
+    CONFIGS[_n + "_mxfp8"] = MoEShape(_n + "_mxfp8", _b.T, _b.D, _b.I, _b.E, _b.k, _b.I_s, _b.score, _b.load,
+                                      precision="mxfp8", config_id=_b.config_id)
 
 
 # --------------------------------------------------------------------------- build / load
