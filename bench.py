@@ -13,8 +13,8 @@ effective TFLOP/s = 6 T (k + 1) D I / t ("Mixture-of-Kittens", Sec. 4.1).
 N > 1 runs N independent replicas (one process per GPU, launched by
 torch.distributed.run): the layer has no data-parallel exchange on one node,
 so value = all replicas' tokens / max-over-ranks time ("scaling": "weak").
---impl reference times the fp64 CPU oracle (the only reference this build
-has) on a bounded token sample per step, on rank 0.
+--impl reference times the fp64 CPU oracle (there is no other reference
+implementation) on a bounded token sample per step, on rank 0.
 """
 from __future__ import annotations
 
