@@ -6,7 +6,9 @@ imports the CUDA library: the two share no code.  Only the seeded input
 generator (``moe_inputs``) serves both.
 
 The arithmetic lives in ``moe_oracle.c`` (plain loops in fp64, OpenMP over
-tokens) and ``alg1.py`` (Algorithm 1 for any number of ranks).  Every function
+tokens), ``alg1.py`` (Algorithm 1 for any number of ranks) and ``backward.py``
+(the layer's backward pass by the chain rule, fp64 numpy, pinned in
+``tests/test_oracle_backward.py``).  Every function
 follows "Mixture-of-Kittens: MoE Megakernel for NVL72s" as cited in those
 files.  Parity status of each function (what pins it) is listed in the tests
 ``tests/test_oracle_pins.py``; absolute layer values beyond those pins have no
