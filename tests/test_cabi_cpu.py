@@ -73,3 +73,26 @@ def test_null_arguments(L):
     assert L.moe_get_status(None, None, ctypes.byref(st), None) == rg.MOE_ERR_INVALID_ARG
     assert L.moe_plan_destroy(None) == 0
     assert L.moe_mxfp8_scale_bytes(128, 64) == 256
+
+
+def test_plan_rejects_bad_knobs(L):
+    # CTA pairs need ring or spread dispatch and even CTA counts; the knobs' ranges
+    base = dict(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
+    for kw in (dict(mma_pair=1, dispatch="direct"), dict(mma_pair=1, gather_ctas=3), dict(mma_pair=1, gemm_ctas=5),
+               dict(mma_pair=1, precision="mxfp8", dispatch="direct"), dict(mma_pair=2), dict(raster=-1),
+               dict(l2_prefetch=65), dict(dispatch=7), dict(gemm_ctas=-1)):
+        with pytest.raises(rg.MoEError) as ei:
+            rg.moe_plan_create(**base, **kw)
+        assert ei.value.code == rg.MOE_ERR_INVALID_ARG, kw
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_knobs_pass_validation(L):
+    # accepted configurations get as far as the device query (which fails without a GPU)
+    base = dict(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
+    for kw in (dict(mma_pair=1), dict(mma_pair=1, precision="mxfp8", dispatch="spread"),
+               dict(mma_pair=1, gather_ctas=3, dispatch="spread"), dict(dispatch="direct", precision="mxfp8"),
+               dict(raster=3, mma_pair=1), dict(k=16, E=512, I_s=0)):
+        with pytest.raises(rg.MoEError) as ei:
+            rg.moe_plan_create(**{**base, **kw})
+        assert ei.value.code in (rg.MOE_ERR_CUDA, rg.MOE_ERR_UNSUPPORTED_DEVICE), kw
