@@ -46,6 +46,7 @@ CALIBRATION_PATH = os.path.join(_REPO, "tests", "golden", "router_calibration.js
 # tensor ids of the counter-based streams
 TID_X, TID_WR, TID_WUP, TID_WGATE, TID_WDOWN = 1, 2, 3, 4, 5
 TID_WS_UP, TID_WS_GATE, TID_WS_DOWN = 6, 7, 8
+TID_DOUT = 9  # upstream gradient dL/d out of a backward pass
 SEED_BASE = 20261202
 
 
@@ -298,6 +299,17 @@ def make_inputs(shape: MoEShape | str, T: int | None = None, weights: bool = Tru
             inp.ws_gate = normal_bf16(seed, TID_WS_GATE, I_s * D, 1.0 / math.sqrt(D)).reshape(I_s, D)
             inp.ws_down = normal_bf16(seed, TID_WS_DOWN, D * I_s, 1.0 / math.sqrt(I_s)).reshape(D, I_s)
     return inp
+
+
+def grad_out(shape: MoEShape | str, T: int | None = None, seed: int | None = None) -> np.ndarray:
+    """Upstream gradient dL/d out of a backward pass: bf16 bit patterns of
+    N(0, 1) draws, [T, D], rows 0..T-1 of the workload's full [shape.T, D]
+    draw (the same rows for any T)."""
+    if isinstance(shape, str):
+        shape = CONFIGS[shape]
+    T = shape.T if T is None else T
+    seed = shape.seed if seed is None else seed
+    return normal_bf16(seed, TID_DOUT, T * shape.D).reshape(T, shape.D)
 
 
 def custom_shape(T: int, D: int, I: int, E: int, k: int, I_s: int, score: str = "sigmoid",

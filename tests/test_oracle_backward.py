@@ -136,3 +136,12 @@ def test_unrouted_expert_gets_no_gradient():
     p["b_router"][5] = -50.0
     g = bw.moe_bwd(p, 2, "sigmoid", np.ones_like(p["x"]))
     assert not g["w_up"][5].any() and not g["w_gate"][5].any() and not g["w_down"][5].any()
+
+
+def test_upstream_gradient_generator():
+    # dL/d out of the backward workloads: N(0, 1) bf16, a prefix of the full draw for any T
+    a, b = mi.grad_out("tiny"), mi.grad_out("tiny", T=100)
+    assert a.shape == (256, 256) and a.dtype == np.uint16 and np.array_equal(a[:100], b)
+    v = f64(a)
+    assert abs(v.mean()) < 0.02 and abs(v.std() - 1.0) < 0.02
+    assert not np.array_equal(a, mi.make_inputs("tiny").x)  # its own stream, not x's
