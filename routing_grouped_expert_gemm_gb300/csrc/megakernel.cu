@@ -373,20 +373,6 @@ __device__ __forceinline__ void release_bar(uint64_t* local, uint32_t remote, bo
 __device__ __forceinline__ void release_acc(const AccRelease& r) { release_bar(r.local, r.remote, r.pair); }
 __device__ __forceinline__ void release_head(const AccRelease& r) { release_bar(r.head_local, r.head_remote, r.pair); }
 
-// 128 threads, thread r owns tile row r (TMEM lane r).
-__device__ __forceinline__ void store_row_bf16x32(bf16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    d[i] = w;
-  }
-}
-
 // Epilogue data movement: each warp owns 32 tile rows (TMEM lanes).  A
 // tcgen05.ld gives lane r the 32 columns of row r; the warp stages that 32x32
 // block in shared memory (row stride 33 floats: conflict-free both ways) and
