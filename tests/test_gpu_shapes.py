@@ -49,7 +49,7 @@ def test_page_shape_bf16_sampled(name):
     g.check_out(g.bf16_dev_to_f64(res["out"])[rows], ref)
 
 
-@pytest.mark.parametrize("name", ["glm52", "qwen35"])
+@pytest.mark.parametrize("name", ["glm52", "qwen35", "kimi_k27", "dsv4pro"])
 def test_page_shape_mxfp8_sampled(name):
     from test_gpu_mxfp8 import check_mx, run_mx
     base = mi.make_inputs(name, T=T_TEST)
