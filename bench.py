@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 sub-measurement")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the minibatch sweep (512 / 2048 / 8192 / 32768 and ring vs over-allocation)")
     ap.add_argument("--gather-ctas-mx", type=int, default=6, help="gather CTAs for the MXFP8 layer")
     ap.add_argument("--dispatch", choices=["ring", "direct", "spread"], default="ring",
                     help="BF16 layer: how the routed tokens reach the expert tiles")
@@ -215,7 +217,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(shape, args, "oracle on host cores"),
+        "config": workload_config(shape, args),
+        "note": "oracle on host cores",
         "tflops": shape.flops(per_step_tokens) * len(times) / total / 1e12,
         "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": value, "unit": "tokens/s",
                          "sample": f"first {per_step_tokens} tokens of the {shape.name} workload per step, fp64"},
@@ -225,7 +228,7 @@ def run_reference(args, world, rank):
     return 0
 
 
-def workload_config(shape, args, extra=None):
+def workload_config(shape, args):
     cfg = {"workload": f"{shape.name}: DeepSeek-V3-shaped MoE layer forward" if shape.name.startswith("dsv3")
            else f"{shape.name} MoE layer forward",
            "T": shape.T, "D": shape.D, "I": shape.I, "E": shape.E, "k": shape.k, "I_s": shape.I_s,
@@ -238,8 +241,6 @@ def workload_config(shape, args, extra=None):
            "gemm_ctas": args.gemm_ctas or "all remaining SMs",
            "l2": "inputs larger than L2 (expert weights 22.5 GB, x 235 MB for dsv3); no flush",
            "parallelism": "replicas"}
-    if extra:
-        cfg["note"] = extra
     return cfg
 
 
@@ -293,18 +294,27 @@ class Runner:
     """One workload on the device: plan, weights (MXFP8 quantised outside any
     timed region), workspace, and a timed loop of moe_fwd calls."""
 
-    def __init__(self, rg, torch, shape, inp, args, world):
+    def __init__(self, rg, torch, shape, inp, args, world, share=None, **knobs):
+        """share: an earlier Runner of the same workload whose device weights and
+        input are reused; knobs: plan settings that replace the arguments'."""
         self.rg, self.torch, self.shape, self.inp, self.args, self.world = rg, torch, shape, inp, args, world
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
         T = shape.T
+        plan_kw = dict(minibatch=args.minibatch, ring_slots=args.ring_slots,
+                       gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8" else args.gather_ctas,
+                       lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
+                       gemm_ctas=args.gemm_ctas, mma_pair=args.mma_pair)
+        plan_kw.update(knobs)
+        self.knobs = plan_kw
         self.plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,
-                                       precision=shape.precision, minibatch=args.minibatch,
-                                       ring_slots=args.ring_slots,
-                                       gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8"
-                                       else args.gather_ctas,
-                                       lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
-                                       gemm_ctas=args.gemm_ctas,
-                                       mma_pair=args.mma_pair)
+                                       precision=shape.precision, **plan_kw)
+        self.stream = torch.cuda.current_stream()
+        self.launches = 3 + (1 if shape.precision == "mxfp8" and plan_kw["dispatch"] == "direct" else 0)
+        self.ws_bytes = rg.moe_workspace_bytes(self.plan, T)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        if share is not None:
+            self.w, self.x, self.out = share.w, share.x, share.out
+            return
         w = {"W_router": dev(inp.w_router),
              "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()}
         for name, arr, rows, K in (("W_up", inp.w_up, shape.E * shape.I, shape.D),
@@ -324,11 +334,7 @@ class Runner:
             w.update(Ws_up=dev(inp.ws_up), Ws_gate=dev(inp.ws_gate), Ws_down=dev(inp.ws_down))
         self.w = w
         self.x = dev(inp.x)
-        self.ws_bytes = rg.moe_workspace_bytes(self.plan, T)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
         self.out = torch.empty((T, shape.D), dtype=torch.bfloat16, device="cuda")
-        self.stream = torch.cuda.current_stream()
-        self.launches = 3 + (1 if shape.precision == "mxfp8" else 0)  # + the per-token x quantisation
 
     def step(self, x=None):
         self.rg.moe_fwd(self.plan, self.shape.T, self.x if x is None else x, self.w, self.out, self.ws,
@@ -371,7 +377,8 @@ class Runner:
         rg.moe_plan_set_timing_events(self.plan, None)
         if self.status() != 0:
             raise SystemExit(f"device status {self.status()} in the timed region")
-        return {"elapsed_ms": start.elapsed_time(end),
+        phases = rg.moe_get_phase_times(self.plan, self.ws, stream=self.stream)  # the last timed launch
+        return {"elapsed_ms": start.elapsed_time(end), "phase_stamps_ms": phases,
                 "router_ms": [e[0].elapsed_time(e[1]) for e in ev],
                 "sched_ms": [e[1].elapsed_time(e[2]) for e in ev],
                 "mega_ms": [e[2].elapsed_time(e[3]) for e in ev],
@@ -436,6 +443,89 @@ class Runner:
         return {"ms": s0.elapsed_time(s1), "h2d": x_host.numel() * 2, "d2h": outs_host[0].numel() * 2}
 
 
+def flops_split(shape, T=None):
+    """(routed, shared) expert-FFN FLOPs of one forward (Sec. 4.1's 6 T k D I
+    and 6 T D I_s)."""
+    T = shape.T if T is None else T
+    return 6.0 * T * shape.k * shape.D * shape.I, 6.0 * T * shape.D * shape.I_s
+
+
+def tensor_roofline(shape, kernel_ms, bf16_peak, peak_src, burst_peak):
+    """Roofline of the persistent kernel: achieved TFLOP/s against the time the
+    work takes at peak.  BF16: every FLOP at the BF16 peak.  MXFP8: the routed
+    FLOPs at 2x the BF16 peak (the dense MXFP8 rate, MoK Sec. 4.1) and the
+    shared expert's (BF16) at 1x, so the peak is the blended rate."""
+    routed, shared = flops_split(shape)
+    total = routed + shared
+    mx = shape.precision == "mxfp8"
+
+    def at_peak_s(p):
+        return (routed / (2.0 * p) if mx else routed / p) + shared / p
+    achieved = total / (kernel_ms / 1000.0) / 1e12
+    blended = total / at_peak_s(bf16_peak * 1e12) / 1e12
+    blended_burst = total / at_peak_s(burst_peak * 1e12) / 1e12
+    return {"kernel": "moe_megakernel", "bound": "tensor", "achieved": achieved, "peak": blended,
+            "unit": "TFLOP/s", "frac": achieved / blended,
+            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)"
+                           + ("; routed FLOPs at 2x (MXFP8 dense), shared-expert FLOPs at 1x (BF16)" if mx else ""),
+            "frac_of_burst_peak": achieved / blended_burst}
+
+
+def phase_bandwidths(shape, res, hbm_peak):
+    """HBM figures of the phases that move data rather than multiply, from the
+    last timed launch: the router's read of x (CUDA events), the ring fill
+    (bytes gathered over the window until the last minibatch was marked
+    gathered; overlapped with the expert tiles and paced by the ring) and the
+    final combine pass (it runs alone: staging rows + g read, output written)."""
+    T, D, k, kY = shape.T, shape.D, shape.k, shape.k + shape.n_shared
+    router_ms = statistics.mean(res["router_ms"])
+    router_bytes = T * D * 2 + shape.E * D * 2
+    fill_bytes = T * k * D * (2 + 2 if shape.precision == "bf16" else 2 + 1 + 1 / 32)
+    comb_bytes = T * kY * D * 2 + T * D * 2 + T * k * 4
+    st = res.get("phase_stamps_ms") or {}
+    out = {"router": {"bytes": router_bytes, "ms": router_ms, "GB/s": router_bytes / router_ms / 1e6}}
+    if st.get("last_fill"):
+        out["ring_fill"] = {"bytes": fill_bytes, "window_ms": st["last_fill"],
+                            "GB/s": fill_bytes / st["last_fill"] / 1e6,
+                            "note": "x rows read + ring rows written (MXFP8: bf16 read, codes + scales written) "
+                                    "over kernel start .. last minibatch gathered; overlapped, paced by the ring"}
+    if st.get("combine_start") is not None and st.get("combine_end") is not None:
+        ms = st["combine_end"] - st["combine_start"]
+        if ms > 0:
+            out["combine"] = {"bytes": comb_bytes, "ms": ms, "GB/s": comb_bytes / ms / 1e6,
+                              "frac_of_hbm_peak": comb_bytes / ms / 1e6 / hbm_peak}
+    out["hbm_peak_GB/s"] = hbm_peak
+    return out
+
+
+def minibatch_sweep(run, steps, warmup):
+    """tokens/s of the same layer (same device weights) at the minibatch sizes
+    MoK Sec. 3.2 sweeps, 4 ring slots each (32768 x 4 holds every route: the
+    over-allocated buffer of Sec. 3.3), and ring vs over-allocation at the
+    default minibatch (4 slots: the ring wraps; T k / b slots: it never does)."""
+    shape = run.shape
+    R = shape.T * shape.k
+    base = run.knobs["minibatch"]
+    points = [(b, 4) for b in (512, 2048, 8192, 32768)]
+    points.append((base, max(4, -(-R // base))))
+    out = []
+    for b, slots in points:
+        r = Runner(run.rg, run.torch, shape, run.inp, run.args, run.world, share=run, minibatch=b, ring_slots=slots)
+        res = r.timed(steps, warmup)
+        out.append({"minibatch": b, "ring_slots": slots, "wraps": slots * b < R,
+                    "tokens_per_s": shape.T * steps / (res["elapsed_ms"] / 1000.0),
+                    "ms_per_step": res["elapsed_ms"] / steps,
+                    "megakernel_ms": statistics.mean(res["mega_ms"])})
+        del r
+    ring = next(p for p in out if p["minibatch"] == base and p["ring_slots"] == 4)
+    full = out[-1]
+    return {"points": out,
+            "ring_vs_overallocation": {"minibatch": base, "ring_ms": ring["ms_per_step"],
+                                       "overallocated_ms": full["ms_per_step"],
+                                       "ring_overhead": ring["ms_per_step"] / full["ms_per_step"] - 1.0},
+            "best_over_worst": max(p["tokens_per_s"] for p in out[:4]) / min(p["tokens_per_s"] for p in out[:4])}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import routing_grouped_expert_gemm_gb300 as rg
@@ -452,6 +542,8 @@ def run_ours(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     bf16_peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    burst_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
 
     t_gen = time.perf_counter()
     shape, inp = select_workload(args)
@@ -466,12 +558,14 @@ def run_ours(args, world, rank, local):
         e2e["ms"] = allmax(e2e["ms"])
         e2e_serial["ms"] = allmax(e2e_serial["ms"])
     flops = shape.flops(T)
-    mx_peak = 2.0 * bf16_peak  # MXFP8 dense peak = 2x BF16 (MoK Sec. 4.1; nominal 4.5 vs 2.25 PFLOP/s)
-    peak = mx_peak if shape.precision == "mxfp8" else bf16_peak
     mega_mean = sum(res["mega_ms"]) / len(res["mega_ms"])
-    achieved = flops / (mega_mean / 1000.0) / 1e12
     cfg = workload_config(shape, args)
+    roof = tensor_roofline(shape, mega_mean, bf16_peak, peak_src, burst_peak)
     traffic = recorded_traffic(f"{shape.name}_{shape.precision}", cfg)
+    roof["traffic"] = traffic
+    roof["traffic_note"] = (("DRAM bytes per launch from a small-case ncu capture scaled to this workload "
+                             "(profiles/traffic_%s_%s.txt)" % (shape.name, shape.precision)) if traffic
+                            else "no ncu capture for these sources and this launch configuration")
     line = {
         "metric": METRIC,
         "value": replica_throughput(world, T, args.steps, elapsed_ms), "unit": "tokens/s", "n_gpus": world,
@@ -484,20 +578,13 @@ def run_ours(args, world, rank, local):
         "ms_median_step": statistics.median(res["step_ms"]),
         "phases_ms_mean": {"router_topk": statistics.mean(res["router_ms"]),
                            "schedule": statistics.mean(res["sched_ms"]), "megakernel": mega_mean},
-        "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "traffic_note": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum, "
-                                     "profiles/traffic_%s_%s.txt)" % (shape.name, shape.precision)
-                                     if traffic else "no ncu capture for these sources and this config",
-                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long loop)"
-                                    + (", x2 for MXFP8" if shape.precision == "mxfp8" else ""),
-                     "frac_of_burst_peak": achieved / (float(peaks["bf16_tflops"])
-                                                       * (2.0 if shape.precision == "mxfp8" else 1.0))},
+        "roofline": roof,
+        "phase_bandwidth": phase_bandwidths(shape, res, hbm_peak),
         "gpu_launches": run.launches * args.steps,
         "clocks": res["clocks"],
         "input_generation_s": t_gen,
     }
-    line["tflops_frac_of_peak"] = line["tflops"] / (world * peak)
+    line["tflops_frac_of_peak"] = line["tflops"] / (world * roof["peak"])
     if e2e:
         # copies on a second stream overlap the neighbouring steps' forwards;
         # "serial": copy in, forward, copy out one after the other
@@ -506,6 +593,10 @@ def run_ours(args, world, rank, local):
                        "copies": "pipelined: input copies, forwards, output copies on three streams, "
                                  "two device input/output buffers",
                        "serial_value": replica_throughput(world, T, args.steps, e2e_serial["ms"])}
+    sweep_steps = max(3, args.steps // 4)
+    full_size = not (args.tokens or args.experts)
+    if not args.no_sweep and full_size:
+        line["minibatch_sweep"] = minibatch_sweep(run, sweep_steps, 3)
     cpu = None
     if world == 1 and not args.no_cpu_baseline and rank == 0:
         cb = time_oracle(inp, args.cpu_seconds)
@@ -515,14 +606,13 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
 
     # the same layer in MXFP8 (routed experts), its own seeded inputs, uniform routing
-    if not args.no_mxfp8 and args.workload == "dsv3" and not (args.tokens or args.experts):
+    if not args.no_mxfp8 and args.workload == "dsv3" and full_size:
         mshape = mi.CONFIGS["dsv3_mxfp8"]
         minp = mi.make_inputs(mshape)
         mrun = Runner(rg, torch, mshape, minp, args, world)
-        mres = mrun.timed(args.steps, args.warmup)
+        mres = mrun.timed(args.steps, args.warmup, ClockSampler(local))
         m_el = allmax(mres["elapsed_ms"])
         m_mega = statistics.mean(mres["mega_ms"])
-        m_ach = mshape.flops() / (m_mega / 1000.0) / 1e12
         line["mxfp8"] = {
             "workload": "dsv3_mxfp8: DSV3 shape, uniform routing, routed experts MXFP8, shared expert BF16",
             "value": replica_throughput(world, mshape.T, args.steps, m_el), "unit": "tokens/s",
@@ -530,11 +620,13 @@ def run_ours(args, world, rank, local):
             "config": workload_config(mshape, args),
             "phases_ms_mean": {"router_topk": statistics.mean(mres["router_ms"]),
                                "schedule": statistics.mean(mres["sched_ms"]), "megakernel": m_mega},
-            "roofline": {"kernel": "moe_megakernel", "bound": "tensor", "achieved": m_ach, "peak": mx_peak,
-                         "unit": "TFLOP/s", "frac": m_ach / mx_peak,
-                         "peak_source": f"{peak_src} bf16 sustained x2 (MXFP8 dense = 2x BF16)"},
+            "roofline": tensor_roofline(mshape, m_mega, bf16_peak, peak_src, burst_peak),
+            "phase_bandwidth": phase_bandwidths(mshape, mres, hbm_peak),
             "gpu_launches": mrun.launches * args.steps,
+            "clocks": mres["clocks"],
         }
+        if not args.no_sweep:
+            line["mxfp8"]["minibatch_sweep"] = minibatch_sweep(mrun, sweep_steps, 3)
         del mrun
     if world > 1:
         import torch.distributed as dist

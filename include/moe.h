@@ -53,7 +53,10 @@ typedef enum moe_error {
 typedef enum moe_device_status {
   MOE_STATUS_OK = 0,
   MOE_STATUS_TIMEOUT = 1,          /* a device-side wait exceeded its limit; outputs are invalid */
-  MOE_STATUS_SCHEDULE_INVALID = 2  /* an expert index out of range or route counts inconsistent */
+  MOE_STATUS_SCHEDULE_INVALID = 2, /* an expert index out of range or route counts inconsistent */
+  MOE_STATUS_STAGING_OVERFLOW = 3  /* the forward completed, but an expert output left the fp16 range of
+                                      the staging rows (|v| > 65504, or NaN) and was saturated: the
+                                      output is finite but not the layer's value */
 } moe_device_status;
 
 typedef enum moe_score_fn { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 } moe_score_fn;
@@ -103,6 +106,12 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              all 256 columns.  Ring or spread dispatch (direct gives
  *              MOE_ERR_INVALID_ARG); gather_ctas must be even.  Results are
  *              bitwise those of the one-CTA tiles.  0: one CTA per tile.
+ *   test_unfilled_minibatch  test hook for the bounded waits, 0 in normal
+ *              use: n >= 1 makes the ring fill never mark minibatch n - 1 as
+ *              gathered, so the expert tiles waiting for it give up after
+ *              timeout_ms and the forward ends with MOE_STATUS_TIMEOUT (the
+ *              kernels return normally, the stream stays usable).  Ring or
+ *              spread dispatch only (direct gives MOE_ERR_INVALID_ARG).
  *   raster     order of an expert segment's up/gate tiles: groups of `raster`
  *              M-tiles, each group sweeping all I/128 column tiles (so a
  *              group's token rows are re-read from L2 while its weight
@@ -131,6 +140,7 @@ typedef struct moe_config {
   int32_t l2_prefetch;
   int32_t mma_pair;
   int32_t raster;
+  int32_t test_unfilled_minibatch;
 } moe_config;
 
 /*
@@ -225,7 +235,9 @@ size_t moe_mxfp8_scale_bytes(int64_t rows, int64_t K);
  *   workspace  device memory of at least moe_workspace_bytes(plan, T) bytes,
  *              256-byte aligned; its contents need no initialisation
  * Launches, in order on `stream`: router + top-k, schedule, persistent
- * forward kernel; with no host synchronisation.  Two calls on identical
+ * forward kernel (three kernels; MXFP8 with direct dispatch adds a per-token
+ * x quantisation pass before the persistent kernel, ring and spread dispatch
+ * quantise x rows on their way into the ring); no host synchronisation.  Two calls on identical
  * inputs give bitwise-identical outputs, also across minibatch, ring_slots,
  * gather_ctas, gemm_ctas and lag settings.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA.
@@ -234,9 +246,11 @@ int moe_fwd(const moe_plan* plan, int64_t T, const void* x, const moe_weights* w
             void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
- * Read the device status word of the last forward that used `workspace`
- * (a moe_device_status).  This call waits for `stream` to finish: it is the
- * one host synchronisation point, taken only when the caller asks.
+ * Read the device status of the last forward that used `workspace` (a
+ * moe_device_status: a failure if one was recorded, else
+ * MOE_STATUS_STAGING_OVERFLOW if that warning was raised, else MOE_STATUS_OK).
+ * This call waits for `stream` to finish: it is the one host synchronisation
+ * point, taken only when the caller asks.
  */
 int moe_get_status(const moe_plan* plan, const void* workspace, int* device_status, moe_stream_t stream);
 
@@ -249,6 +263,17 @@ int moe_get_status(const moe_plan* plan, const void* workspace, int* device_stat
  * thread runs moe_fwd with the same plan.
  */
 int moe_plan_set_timing_events(moe_plan* plan, void* const* events);
+
+/*
+ * Optional phase timing for profiling harnesses: the persistent kernel of the
+ * last forward that used `workspace` stamps, with the GPU's global timer, when
+ * its first CTA started, when the last minibatch was marked gathered (ring or
+ * spread dispatch), and when the final combine pass began (the first CTA to
+ * start it) and ended (the last CTA to finish it).  times_ms[0..2] receive the
+ * last three as milliseconds after the start (-1 where a phase did not
+ * happen).  Like moe_get_status, this call waits for `stream` to finish.
+ */
+int moe_get_phase_times(const moe_plan* plan, const void* workspace, double* times_ms, moe_stream_t stream);
 
 /*
  * Routing stage without any device allocation -- no counterpart in the paper.

@@ -22,6 +22,9 @@ if os.environ.get("MOE_TRACE_BUILD") == "1":  # profiling only: the MOE_TRACE va
 elif os.environ.get("MOE_DEBUG_BUILD") == "1":  # debugging only: the MOE_DEBUG_LOG variant
     LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300_dbg.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+TESTING_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe_testing.h")
+# test hooks (one-tile probes of tensor-core encodings), a library of their own
+TESTING_LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_gb300_testing.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -31,7 +34,7 @@ MOE_ERR_CUDA = -4
 MOE_ERR_UNSUPPORTED_DEVICE = -5
 MOE_ERR_STATIC_SCRATCH_TOO_SMALL = -6
 MOE_ROUTE_STATIC_MAX_TOKENS = 16384
-MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID = 0, 1, 2
+MOE_STATUS_OK, MOE_STATUS_TIMEOUT, MOE_STATUS_SCHEDULE_INVALID, MOE_STATUS_STAGING_OVERFLOW = 0, 1, 2, 3
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_PREC_BF16, MOE_PREC_MXFP8 = 0, 1
 MOE_DISPATCH_RING, MOE_DISPATCH_DIRECT, MOE_DISPATCH_SPREAD = 0, 1, 2
@@ -49,7 +52,8 @@ class moe_config(ctypes.Structure):
                 ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
                 ("gather_ctas", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32), ("lag", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("dispatch", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
-                ("mma_pair", ctypes.c_int32), ("raster", ctypes.c_int32)]
+                ("mma_pair", ctypes.c_int32), ("raster", ctypes.c_int32),
+                ("test_unfilled_minibatch", ctypes.c_int32)]
 
 
 class moe_weights(ctypes.Structure):
@@ -91,10 +95,30 @@ def lib():
     L.moe_get_status.restype = ctypes.c_int
     L.moe_plan_set_timing_events.argtypes = [vp, ctypes.POINTER(vp)]
     L.moe_plan_set_timing_events.restype = ctypes.c_int
+    L.moe_get_phase_times.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double), vp]
+    L.moe_get_phase_times.restype = ctypes.c_int
     L.moe_route_static.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_route_static.restype = ctypes.c_int
     L.moe_route_static_scratch_bytes.argtypes = []
     L.moe_route_static_scratch_bytes.restype = sz
+    L.moe_error_string.argtypes = [ctypes.c_int]
+    L.moe_error_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+_testing_lib = None
+
+
+def testing_lib():
+    """The test-hook library (one-tile probes; raises if it was not built)."""
+    global _testing_lib
+    if _testing_lib is not None:
+        return _testing_lib
+    if not os.path.exists(TESTING_LIB_PATH):
+        raise RuntimeError(f"test-hook library not built: {TESTING_LIB_PATH} is missing")
+    L = ctypes.CDLL(TESTING_LIB_PATH)
+    vp = ctypes.c_void_p
     L.moe_testing_mx_tile.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_mx_tile.restype = ctypes.c_int
     L.moe_testing_pair_tile.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp]
@@ -103,16 +127,13 @@ def lib():
     L.moe_testing_pair_mma_time.restype = ctypes.c_int
     L.moe_testing_pair_mx_tile.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_pair_mx_tile.restype = ctypes.c_int
-    L.moe_error_string.argtypes = [ctypes.c_int]
-    L.moe_error_string.restype = ctypes.c_char_p
-    _lib = L
+    _testing_lib = L
     return L
 
 
-def declared_functions() -> list[str]:
-    """Function names declared in include/*.h (the ABI and the test hooks)."""
-    inc = os.path.dirname(HEADER_PATH)
-    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
+def declared_functions(header: str | None = None) -> list[str]:
+    """Function names declared in one header (default: include/moe.h, the ABI)."""
+    text = open(header or HEADER_PATH).read()
     return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)))
 
 
@@ -152,7 +173,7 @@ class Plan:
 
 def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
                     ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0, dispatch=MOE_DISPATCH_RING,
-                    l2_prefetch=0, mma_pair=0, raster=0) -> Plan:
+                    l2_prefetch=0, mma_pair=0, raster=0, test_unfilled_minibatch=0) -> Plan:
     if isinstance(score_fn, str):
         score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
     if isinstance(precision, str):
@@ -160,7 +181,7 @@ def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precis
     if isinstance(dispatch, str):
         dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT, "spread": MOE_DISPATCH_SPREAD}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
-                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster)
+                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster, test_unfilled_minibatch)
     h = ctypes.c_void_p()
     rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
     if rc != MOE_OK:
@@ -209,6 +230,17 @@ def moe_get_status(plan: Plan, workspace, stream=None) -> int:
     if rc != MOE_OK:
         raise MoEError(rc, "moe_get_status")
     return st.value
+
+
+def moe_get_phase_times(plan: Plan, workspace, stream=None) -> dict:
+    """Phase stamps of the last forward on ``workspace`` (ms after the persistent
+    kernel's start; None where the phase did not happen)."""
+    arr = (ctypes.c_double * 3)()
+    rc = lib().moe_get_phase_times(plan.handle, _ptr(workspace), arr, _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_get_phase_times")
+    keys = ("last_fill", "combine_start", "combine_end")
+    return {k: (None if v < 0 else float(v)) for k, v in zip(keys, arr)}
 
 
 def moe_plan_set_timing_events(plan: Plan, events) -> None:

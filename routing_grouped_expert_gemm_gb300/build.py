@@ -1,9 +1,13 @@
-"""Build the CUDA library in-tree: csrc/*.cu -> _lib/libmoe_gb300.so (sm_103a).
+"""Build the CUDA libraries in-tree (sm_103a):
+
+  _lib/libmoe_gb300.so          the product: the C ABI of include/moe.h
+  _lib/libmoe_gb300_testing.so  test hooks only (include/moe_testing.h): one-tile
+                                probes that pin tensor-core encodings on the GPU
 
 Each translation unit is compiled in parallel with nvcc
-(-gencode arch=compute_103a,code=sm_103a -lineinfo -O3) and linked into one
-shared library with the CUDA runtime linked statically, so the library loads
-without a GPU (the CPU tests check its exports) and needs no libcuda at link
+(-gencode arch=compute_103a,code=sm_103a -lineinfo -O3) and linked into a
+shared library with the CUDA runtime linked statically, so the libraries load
+without a GPU (the CPU tests check their exports) and need no libcuda at link
 time (the TMA encoder is fetched through the runtime's driver entry point).
 """
 from __future__ import annotations
@@ -19,10 +23,11 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
+TESTING_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_testing.so")
 TRACE_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_trace.so")
 DEBUG_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_dbg.so")
-SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu", "probe_mx.cu",
-           "probe_pair.cu"]
+SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu"]
+TESTING_SOURCES = ["probe_mx.cu", "probe_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -56,27 +61,36 @@ def _stale(lib_path: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False,
-          debug_log: bool = False) -> str:
-    """Build the library; trace=True builds the MOE_TRACE variant (per-CTA wait
-    timers in the persistent kernel) as _lib/libmoe_gb300_trace.so instead;
-    debug_log=True the MOE_DEBUG_LOG variant (per-CTA progress records and
-    bounds checks written to host memory) as _lib/libmoe_gb300_dbg.so."""
-    lib_path = TRACE_LIB_PATH if trace else (DEBUG_LIB_PATH if debug_log else LIB_PATH)
-    obj_dir = OBJ + ("_trace" if trace else ("_dbg" if debug_log else ""))
-    if not force and not _stale(lib_path):
-        return lib_path
-    os.makedirs(obj_dir, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
-    defines = ("MOE_TRACE",) if trace else (("MOE_DEBUG_LOG",) if debug_log else ())
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, ptxas_v, defines, obj_dir), SOURCES))
+def _link(objs, lib_path):
     tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp, "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stderr)
     os.replace(tmp, lib_path)
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, trace: bool = False,
+          debug_log: bool = False) -> str:
+    """Build the library (and, for the plain build, the test-hook library
+    beside it); trace=True builds the MOE_TRACE variant (per-CTA wait timers
+    in the persistent kernel) as _lib/libmoe_gb300_trace.so instead;
+    debug_log=True the MOE_DEBUG_LOG variant (per-CTA progress records and
+    bounds checks written to host memory) as _lib/libmoe_gb300_dbg.so."""
+    lib_path = TRACE_LIB_PATH if trace else (DEBUG_LIB_PATH if debug_log else LIB_PATH)
+    obj_dir = OBJ + ("_trace" if trace else ("_dbg" if debug_log else ""))
+    with_testing = not trace and not debug_log
+    if not force and not _stale(lib_path) and not (with_testing and _stale(TESTING_LIB_PATH)):
+        return lib_path
+    os.makedirs(obj_dir, exist_ok=True)
+    os.makedirs(LIB_DIR, exist_ok=True)
+    defines = ("MOE_TRACE",) if trace else (("MOE_DEBUG_LOG",) if debug_log else ())
+    srcs = SOURCES + (TESTING_SOURCES if with_testing else [])
+    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        objs = dict(zip(srcs, ex.map(lambda s: _compile(s, verbose, ptxas_v, defines, obj_dir), srcs)))
+    _link([objs[s] for s in SOURCES], lib_path)
+    if with_testing:
+        _link([objs[s] for s in TESTING_SOURCES], TESTING_LIB_PATH)
     return lib_path
 
 

@@ -56,7 +56,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
     off = align_up(off + bytes, kAlign);
     return at;
   };
-  L.status = take(sizeof(int));
+  L.status = take(STATUS_AREA_BYTES);  // status word, warning bits, phase stamps
   L.counters = take(sizeof(int) * L.n_counters);
   L.meta = take(sizeof(int) * (META_MB + 4 * L.n_mb));
   L.topk_idx = take(sizeof(int) * L.R);
@@ -76,8 +76,10 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.ring_x = take(direct ? 0 : (size_t)ring_rows * c.D * elem);
   L.ring_h = take((size_t)ring_rows * c.I * elem);
   L.sfx = take(mx && !direct ? (size_t)L.n_mtiles_max * (c.D / BK_MX) * SF_BLOCK_BYTES : 0);
-  L.xq = take(mx ? (size_t)T * c.D : 0);  // x quantised once per token (both dispatch modes)
-  L.xs = take(mx ? (size_t)T * (c.D / 32) : 0);
+  // direct dispatch: x quantised once per token before the persistent kernel
+  // (ring and spread dispatch quantise the rows on their way into the ring)
+  L.xq = take(mx && direct ? (size_t)T * c.D : 0);
+  L.xs = take(mx && direct ? (size_t)T * (c.D / 32) : 0);
   L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
   L.Y = take((size_t)L.n_chunks * BM * (c.k + (c.I_s > 0 ? 1 : 0)) * c.D * 2);  // blocked by token tile, see FwdParams::Y
@@ -170,6 +172,9 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.raster < 0) return MOE_ERR_INVALID_ARG;
   if (c.raster == 0) c.raster = 1 << 20;  // default: column-tile major over the whole segment
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
+  // the test hook needs a ring whose fill is signalled (ring or spread dispatch)
+  if (c.test_unfilled_minibatch < 0 || (c.test_unfilled_minibatch > 0 && c.dispatch == MOE_DISPATCH_DIRECT))
+    return MOE_ERR_INVALID_ARG;
   if (c.mma_pair) c.raster = (c.raster + 1) & ~1;  // a pair's two tasks share a column tile
   if (c.dispatch == MOE_DISPATCH_SPREAD) c.gather_ctas = 0;  // the GEMM CTAs' spare warps gather
   if (c.mma_pair && (c.dispatch == MOE_DISPATCH_DIRECT || (c.gather_ctas & 1) ||
@@ -220,6 +225,23 @@ int moe_plan_set_timing_events(moe_plan* plan, void* const* events) {
     plan->timing[i] = static_cast<cudaEvent_t>(events[i]);
   }
   plan->timed = true;
+  return MOE_OK;
+}
+
+int moe_get_phase_times(const moe_plan* plan, const void* workspace, double* times_ms, moe_stream_t stream) {
+  if (!plan || !workspace || !times_ms) return MOE_ERR_INVALID_ARG;
+  unsigned long long st[N_STAMPS];
+  const uint8_t* area = static_cast<const uint8_t*>(workspace) + 8;
+  if (cudaMemcpyAsync(st, area, sizeof(st), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const unsigned long long t0 = st[STAMP_START];
+  auto rel = [&](unsigned long long v) {
+    return (v == 0ull || v == ~0ull || t0 == ~0ull || v < t0) ? -1.0 : (double)(v - t0) * 1e-6;
+  };
+  times_ms[0] = rel(st[STAMP_LAST_FILL]);
+  times_ms[1] = rel(st[STAMP_COMBINE_START]);
+  times_ms[2] = rel(st[STAMP_COMBINE_END]);
   return MOE_OK;
 }
 
@@ -304,9 +326,11 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.n_counters = (int)L.n_counters;
   p.timeout_ns = (long long)c.timeout_ms * 1000000LL;
   p.l2_prefetch = c.l2_prefetch;
+  p.test_unfilled = c.test_unfilled_minibatch;
   p.x = static_cast<const bf16*>(x);
   p.b_router = w->b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);
+  p.stamps = reinterpret_cast<unsigned long long*>(ws + L.status + 8);
   p.counters = reinterpret_cast<int*>(ws + L.counters);
   p.meta = reinterpret_cast<int*>(ws + L.meta);
   p.topk_idx = reinterpret_cast<int*>(ws + L.topk_idx);
@@ -321,8 +345,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.tasks = reinterpret_cast<Task*>(ws + L.tasks);
   p.ring_x = reinterpret_cast<bf16*>(ws + L.ring_x);
   p.ring_h = reinterpret_cast<bf16*>(ws + L.ring_h);
-  p.xq = mx ? ws + L.xq : nullptr;
-  p.xs = mx ? ws + L.xs : nullptr;
+  p.xq = mx && p.direct ? ws + L.xq : nullptr;
+  p.xs = mx && p.direct ? ws + L.xs : nullptr;
   p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
   p.sfh = mx ? ws + L.sfh : nullptr;
   p.w_up_sf = mx ? w->W_up_scale : nullptr;
@@ -392,7 +416,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   if (pl->timed && cudaEventRecord(pl->timing[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_schedule(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (mx && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
+  if (mx && p.direct && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_megakernel(tm, p, pl->grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -410,11 +434,11 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
 
 int moe_get_status(const moe_plan* plan, const void* workspace, int* device_status, moe_stream_t stream) {
   if (!plan || !workspace || !device_status) return MOE_ERR_INVALID_ARG;
-  int v = 0;
-  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+  int v[2] = {0, 0};  // the status word and the warning bits after it
+  if (cudaMemcpyAsync(v, workspace, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
-  *device_status = v;
+  *device_status = v[0] != STATUS_OK ? v[0] : ((v[1] & FLAG_STAGING_OVERFLOW) ? MOE_STATUS_STAGING_OVERFLOW : MOE_STATUS_OK);
   return MOE_OK;
 }
 

@@ -53,6 +53,15 @@ constexpr int E_MAX = 512;
 
 // device status codes (written to the workspace status word)
 enum : int { STATUS_OK = 0, STATUS_TIMEOUT = 1, STATUS_SCHEDULE_INVALID = 2 };
+// sticky warning bits in the word after the status word: they do not stop the
+// forward (the status word does), they only qualify its result
+enum : int { FLAG_STAGING_OVERFLOW = 1 };
+
+// phase stamps of one persistent-kernel launch (ns of %globaltimer), for
+// per-phase bandwidth figures: the first CTA's start, the last ring fill, the
+// first CTA to start the combine and the last to finish it
+enum : int { STAMP_START = 0, STAMP_LAST_FILL = 1, STAMP_COMBINE_START = 2, STAMP_COMBINE_END = 3, N_STAMPS = 4 };
+constexpr int STATUS_AREA_BYTES = 256;  // status word, warning bits (8 B), then the stamps (8-byte aligned)
 
 // task kinds of the persistent kernel
 enum : int { TASK_R1 = 0, TASK_R2 = 1, TASK_S1 = 2, TASK_S2 = 3 };
@@ -96,12 +105,14 @@ struct FwdParams {
   int n_mtiles_max, n_smtiles, n_tasks_max;
   int n_counters;
   int l2_prefetch;      // K steps ahead that the producer prefetches into L2 (0 = off)
+  int test_unfilled;    // test hook: 0 off; m + 1 = minibatch m is never marked gathered
   long long timeout_ns;
   // inputs
   const bf16* x;
   const float* b_router;
   // workspace sections
-  int* status;
+  int* status;        // [0] moe_device_status, [1] FLAG_* warning bits; both zeroed by the router kernel
+  unsigned long long* stamps;  // [STAMP_*] %globaltimer phase stamps of the persistent kernel (reset by the router)
   int* counters;      // zeroed by the router kernel
   int* meta;
   int* topk_idx;      // [T,k]

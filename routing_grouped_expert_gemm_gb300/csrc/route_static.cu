@@ -55,36 +55,42 @@ int scratch_address(int dev, void** out) {
   return MOE_OK;
 }
 
-size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct RouteLayout {
   size_t status, counters, meta, chunk_counts, mtiles, segs, total;
   int n_mb, n_chunks, max_segs, n_mtiles_max, n_counters;
 };
 
-RouteLayout route_layout(int64_t T, int64_t E, int64_t k) {
+// Scratch layout of one call; the counter block has the size the kernels
+// index (n_counters() of the persistent kernel's layout, no shared tiles).
+constexpr RouteLayout route_layout(int64_t T, int64_t E, int64_t k) {
   RouteLayout L{};
   const int64_t R = T * k;
   L.n_mb = (int)((R + kRouteMinibatch - 1) / kRouteMinibatch);
   L.n_chunks = (int)((T + BM - 1) / BM);
   L.max_segs = L.n_mb + (int)E;
   L.n_mtiles_max = (int)((R + BM - 1) / BM) + L.n_mb + (int)E;
-  L.n_counters = 1 + 3 * L.n_mb + L.n_mtiles_max;
+  L.n_counters = 2 + 3 * L.n_mb + L.n_mtiles_max;
   size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = off;
-    off = align256(off + bytes);
-    return at;
-  };
-  L.status = take(sizeof(int));
-  L.counters = take(sizeof(int) * (size_t)L.n_counters);
-  L.meta = take(sizeof(int) * (size_t)(META_MB + 4 * L.n_mb));
-  L.chunk_counts = take(sizeof(int) * (size_t)L.n_chunks * (size_t)E);
-  L.mtiles = take(sizeof(int) * 4 * (size_t)L.n_mtiles_max);
-  L.segs = take(sizeof(int) * (size_t)(4 * L.max_segs + 4 * (2 * L.max_segs + 2) + L.n_mb + 1));
+  L.status = off;  // status word, warning bits, phase stamps
+  off = align256(off + STATUS_AREA_BYTES);
+  L.counters = off;
+  off = align256(off + sizeof(int) * (size_t)L.n_counters);
+  L.meta = off;
+  off = align256(off + sizeof(int) * (size_t)(META_MB + 4 * L.n_mb));
+  L.chunk_counts = off;
+  off = align256(off + sizeof(int) * (size_t)L.n_chunks * (size_t)E);
+  L.mtiles = off;
+  off = align256(off + sizeof(int) * 4 * (size_t)L.n_mtiles_max);
+  L.segs = off;
+  off = align256(off + sizeof(int) * (size_t)(4 * L.max_segs + 4 * (2 * L.max_segs + 2) + L.n_mb + 1));
   L.total = off;
   return L;
 }
+// the documented limits fit the fixed array
+static_assert(route_layout(MOE_ROUTE_STATIC_MAX_TOKENS, E_MAX, TOPK_MAX).total <= kRouteScratchBytes,
+              "routing scratch too small for T = MOE_ROUTE_STATIC_MAX_TOKENS, E = 512, k = 16");
 
 int encode_rows(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   cuuint64_t dims[2] = {cols, rows};
@@ -150,6 +156,7 @@ extern "C" int moe_route_static(const moe_plan* pl, int64_t T, const void* x, co
   p.x = static_cast<const bf16*>(x);
   p.b_router = b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);
+  p.stamps = nullptr;  // no persistent kernel
   p.counters = reinterpret_cast<int*>(ws + L.counters);
   p.meta = reinterpret_cast<int*>(ws + L.meta);
   p.chunk_counts = reinterpret_cast<int*>(ws + L.chunk_counts);

@@ -43,7 +43,14 @@ __global__ void __launch_bounds__(ROUTER_THREADS, 1)
   // counters / status of this forward start at zero
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_counters; i += gridDim.x * blockDim.x)
     p.counters[i] = 0;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    p.status[0] = 0;
+    p.status[1] = 0;
+    if (p.stamps) {
+      p.stamps[STAMP_START] = p.stamps[STAMP_COMBINE_START] = ~0ull;
+      p.stamps[STAMP_LAST_FILL] = p.stamps[STAMP_COMBINE_END] = 0ull;
+    }
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     s_hist[e] = 0;
     s_beta[e] = p.b_router ? p.b_router[e] : 0.0f;

@@ -20,12 +20,21 @@ def bf16_dev_to_f64(t: torch.Tensor) -> np.ndarray:
 class Layer:
     """Device copies of one workload's parameters plus a plan and workspace."""
 
-    def __init__(self, inp: mi.MoEInputs, T_max: int | None = None, shared: bool = True, **plan_kw):
+    def __init__(self, inp: mi.MoEInputs, T_max: int | None = None, shared: bool = True, weights: dict | None = None,
+                 **plan_kw):
+        """weights: the device parameters of an earlier Layer of the same
+        workload (shared instead of uploaded again)."""
         s = inp.shape
         self.shape = s
         self.T_max = T_max or inp.T
         self.plan = rg.moe_plan_create(self.T_max, s.D, s.I, s.E, s.k, s.I_s, score_fn=s.score,
                                        precision=s.precision, **plan_kw)
+        self.mx = s.precision == "mxfp8"
+        if weights is not None:
+            self.w = weights
+            self.ws_bytes = rg.moe_workspace_bytes(self.plan, self.T_max)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+            return
         self.w = {
             "W_router": to_dev_bf16(inp.w_router),
             "b_router": None if inp.b_router is None else torch.from_numpy(inp.b_router).to("cuda"),
@@ -33,7 +42,6 @@ class Layer:
             "W_gate": to_dev_bf16(inp.w_gate),
             "W_down": to_dev_bf16(inp.w_down),
         }
-        self.mx = s.precision == "mxfp8"
         if self.mx:  # routed weights quantised on the GPU (codes + scale blocks)
             self.w_bf16 = {k: self.w[k] for k in ("W_up", "W_gate", "W_down")}
             for name, rows, K in (("W_up", s.E * s.I, s.D), ("W_gate", s.E * s.I, s.D), ("W_down", s.E * s.D, s.I)):

@@ -18,19 +18,36 @@ def L():
 
 EXPECTED = {"moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_quantize_mxfp8",
             "moe_mxfp8_scale_bytes", "moe_fwd", "moe_get_status", "moe_error_string",
-            "moe_plan_set_timing_events"}
+            "moe_plan_set_timing_events", "moe_get_phase_times", "moe_route_static", "moe_route_static_scratch_bytes"}
 
 
 def test_header_declares_the_boundary():
     assert EXPECTED <= set(rg.declared_functions())
 
 
+def _exported(path):
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if " T " in line}
+
+
 def test_library_exports_every_declared_function(L):
-    out = subprocess.run(["nm", "-D", "--defined-only", rg.LIB_PATH], capture_output=True, text=True).stdout
-    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    exported = _exported(rg.LIB_PATH)
     for name in rg.declared_functions():
         assert name in exported, name
         assert getattr(L, name) is not None
+
+
+def test_test_hooks_live_in_their_own_library(L):
+    """The one-tile probes (include/moe_testing.h) ship in the test-hook
+    library only; the product library exports none of them."""
+    hooks = rg.declared_functions(rg.TESTING_HEADER_PATH)
+    assert hooks and all(h.startswith("moe_testing_") for h in hooks)
+    exported = _exported(rg.TESTING_LIB_PATH)
+    T = rg.testing_lib()
+    for name in hooks:
+        assert name in exported, name
+        assert getattr(T, name) is not None
+    assert not any(n.startswith("moe_testing_") for n in _exported(rg.LIB_PATH))
 
 
 def test_error_strings(L):
@@ -80,7 +97,8 @@ def test_plan_rejects_bad_knobs(L):
     base = dict(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
     for kw in (dict(mma_pair=1, dispatch="direct"), dict(mma_pair=1, gather_ctas=3), dict(mma_pair=1, gemm_ctas=5),
                dict(mma_pair=1, precision="mxfp8", dispatch="direct"), dict(mma_pair=2), dict(raster=-1),
-               dict(l2_prefetch=65), dict(dispatch=7), dict(gemm_ctas=-1)):
+               dict(l2_prefetch=65), dict(dispatch=7), dict(gemm_ctas=-1),
+               dict(test_unfilled_minibatch=-1), dict(test_unfilled_minibatch=1, dispatch="direct")):
         with pytest.raises(rg.MoEError) as ei:
             rg.moe_plan_create(**base, **kw)
         assert ei.value.code == rg.MOE_ERR_INVALID_ARG, kw
@@ -92,7 +110,8 @@ def test_valid_knobs_pass_validation(L):
     base = dict(T_max=256, D=256, I=128, E=16, k=4, I_s=128)
     for kw in (dict(mma_pair=1), dict(mma_pair=1, precision="mxfp8", dispatch="spread"),
                dict(mma_pair=1, gather_ctas=3, dispatch="spread"), dict(dispatch="direct", precision="mxfp8"),
-               dict(raster=3, mma_pair=1), dict(k=16, E=512, I_s=0)):
+               dict(raster=3, mma_pair=1), dict(k=16, E=512, I_s=0), dict(test_unfilled_minibatch=1),
+               dict(test_unfilled_minibatch=2, dispatch="spread")):
         with pytest.raises(rg.MoEError) as ei:
             rg.moe_plan_create(**{**base, **kw})
         assert ei.value.code in (rg.MOE_ERR_CUDA, rg.MOE_ERR_UNSUPPORTED_DEVICE), kw

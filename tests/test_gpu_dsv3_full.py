@@ -1,0 +1,169 @@
+"""The DeepSeek-V3-shaped layer at full size (T = 16384, D = 7168, I = 2048,
+E = 256, k = 8, one shared expert) through the C ABI, against the fp64 oracle.
+
+BF16 with the Zipf(1.1) expert load, MXFP8 routed experts with the uniform
+load.  For each precision one set of device weights serves every launch
+configuration: the benchmark's (CTA pairs; ring dispatch with 8 gather CTAs
+for BF16, spread for MXFP8), the minibatch sizes 512, 2048 and 32768 that
+"Mixture-of-Kittens: MoE Megakernel for NVL72s" sweeps (Sec. 3.2, Fig. 5;
+32768 x 4 ring slots holds all T*k routes: the over-allocated buffer of
+Sec. 3.3), and the one-CTA kernel with each dispatch mode.
+
+Bars: routing (top-k, g, counts, offsets, schedule, its inverse) on every
+token; outputs on a 1024-token sample that holds every token routed to the
+eight experts with the fewest routes, the tokens of the first and last M-tile
+of the schedule (the last minibatch's tail) and tokens spread over the rest,
+at rel-L2 <= 1e-2 and max-abs <= 3e-2 rms(out) for BF16 (MXFP8: rel-L2 <= 1e-2
+against the oracle on the same quantised values, <= 6e-2 against the
+unquantised oracle); and every configuration's whole output bitwise equal to
+the benchmark configuration's, which is itself bitwise equal on a repeat run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE = 1024
+
+BF16_CONFIGS = [  # (name, plan knobs); the first is the benchmark's
+    ("bench", dict(minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("b512", dict(minibatch=512, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("b2048", dict(minibatch=2048, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("b32768x4", dict(minibatch=32768, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("one_cta_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=8)),
+    ("one_cta_direct", dict(minibatch=8192, ring_slots=4, dispatch="direct")),
+    ("one_cta_spread", dict(minibatch=8192, ring_slots=4, dispatch="spread")),
+]
+MX_CONFIGS = [
+    ("bench", dict(minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)),
+    ("b512", dict(minibatch=512, ring_slots=4, dispatch="spread", mma_pair=1)),
+    ("b2048", dict(minibatch=2048, ring_slots=4, dispatch="spread", mma_pair=1)),
+    ("b32768x4", dict(minibatch=32768, ring_slots=4, dispatch="spread", mma_pair=1)),
+    ("pair_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=6, mma_pair=1)),
+    ("one_cta_direct", dict(minibatch=8192, ring_slots=4, dispatch="direct")),
+    ("one_cta_spread", dict(minibatch=8192, ring_slots=4, dispatch="spread")),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from routing_grouped_expert_gemm_gb300 import build
+    build.build()
+
+
+class Workload:
+    """One workload's inputs, device weights, routing oracle and sample."""
+
+    def __init__(self, name):
+        import gpu_util
+        self.inp = mi.make_inputs(name)
+        s = self.inp.shape
+        self.x = gpu_util.to_dev_bf16(self.inp.x)
+        first = gpu_util.Layer(self.inp, **(BF16_CONFIGS if s.precision == "bf16" else MX_CONFIGS)[0][1])
+        self.weights = first.w
+        del first
+        logits = oracle.router_logits(self.inp.x, self.inp.w_router, self.inp.b_router)
+        self.idx_ref, self.g_ref = oracle.topk(logits, s.k, s.score)
+        M, _, sched, _ = oracle.schedule(self.idx_ref, s.E)
+        self.rows = sample_rows(self.idx_ref, M, sched, s.T)
+        self.bits = {}
+
+
+def sample_rows(idx, M, sched, T, n=N_SAMPLE):
+    """Tokens routed to the eight experts with the fewest (non-zero) routes,
+    the tokens of the first and last 128 schedule rows, then evenly spaced
+    tokens, up to n distinct tokens (sorted)."""
+    tail_experts = [e for e in np.argsort(M, kind="stable") if M[e] > 0][:8]
+    picked = list(np.nonzero(np.isin(idx, tail_experts).any(axis=1))[0])
+    picked += list(sched[:128, 0]) + list(sched[-128:, 0])
+    rows = np.unique(np.asarray(picked, dtype=np.int64))[:n]
+    if len(rows) < n:
+        spread = np.linspace(0, T - 1, 4 * n).astype(np.int64)
+        extra = np.setdiff1d(spread, rows)[: n - len(rows)]
+        rows = np.union1d(rows, extra)
+    return rows
+
+
+_cache = {}
+
+
+def workload(name):
+    if name not in _cache:
+        _cache.clear()  # one workload's weights on the device at a time
+        torch.cuda.empty_cache()
+        _cache[name] = Workload(name)
+    return _cache[name]
+
+
+def run_config(w, knobs):
+    import gpu_util
+    from test_gpu_parity import compare_routing
+    layer = gpu_util.Layer(w.inp, weights=w.weights, **knobs)
+    res = layer.run(w.x)
+    assert res["status"] == 0
+    compare_routing(res, w.idx_ref, w.g_ref, w.inp.shape.E)
+    del layer
+    return res
+
+
+# ----------------------------------------------------------------------------- BF16, Zipf load
+@pytest.fixture(scope="module")
+def dsv3_ref():
+    w = workload("dsv3")
+    ref, _, _ = oracle.moe_fwd_inputs(w.inp, rows=w.rows)
+    return ref
+
+
+@pytest.mark.parametrize("name,knobs", BF16_CONFIGS, ids=[c[0] for c in BF16_CONFIGS])
+def test_dsv3_bf16(name, knobs, dsv3_ref):
+    import gpu_util
+    w = workload("dsv3")
+    res = run_config(w, knobs)
+    got = gpu_util.bf16_dev_to_f64(res["out"])[w.rows]
+    gpu_util.check_out(got, dsv3_ref)
+    bits = res["out"].view(torch.int16).cpu().numpy()
+    if name == "bench":  # repeat run of the benchmark configuration: the same bits
+        again = run_config(w, knobs)["out"].view(torch.int16).cpu().numpy()
+        assert np.array_equal(bits, again), "repeat run differs"
+        w.bits["bench"] = bits
+    else:
+        assert "bench" in w.bits
+        assert np.array_equal(bits, w.bits["bench"]), f"{name}: output bits differ from the benchmark configuration"
+
+
+# ----------------------------------------------------------------------------- MXFP8, uniform load
+@pytest.fixture(scope="module")
+def dsv3_mx_ref():
+    from test_gpu_mxfp8 import oracle_mx_weights
+    w = workload("dsv3_mxfp8")
+    mx = oracle_mx_weights(w.inp)
+    ref_mx, _, _ = oracle.moe_fwd_inputs(w.inp, rows=w.rows, mx=mx)
+    ref_bf, _, _ = oracle.moe_fwd_inputs(w.inp, rows=w.rows)
+    return ref_mx, ref_bf
+
+
+@pytest.mark.parametrize("name,knobs", MX_CONFIGS, ids=[c[0] for c in MX_CONFIGS])
+def test_dsv3_mxfp8(name, knobs, dsv3_mx_ref):
+    import gpu_util
+    w = workload("dsv3_mxfp8")
+    res = run_config(w, knobs)
+    got = gpu_util.bf16_dev_to_f64(res["out"])[w.rows]
+    assert np.isfinite(got).all()
+    ref_mx, ref_bf = dsv3_mx_ref
+    rel_mx, rel_bf = gpu_util.rel_l2(got, ref_mx), gpu_util.rel_l2(got, ref_bf)
+    assert rel_mx <= 1e-2, f"rel-L2 vs the MX oracle {rel_mx:.3g}"
+    assert rel_bf <= 6e-2, f"rel-L2 vs the unquantised oracle {rel_bf:.3g}"
+    bits = res["out"].view(torch.int16).cpu().numpy()
+    if name == "bench":
+        again = run_config(w, knobs)["out"].view(torch.int16).cpu().numpy()
+        assert np.array_equal(bits, again), "repeat run differs"
+        w.bits["bench"] = bits
+    else:
+        assert "bench" in w.bits
+        assert np.array_equal(bits, w.bits["bench"]), f"{name}: output bits differ from the benchmark configuration"

@@ -71,7 +71,7 @@ def run_probe(A, B, img, mode=0):
     dB = torch.from_numpy(B).cuda()
     dI = torch.from_numpy(np.ascontiguousarray(img).view(np.uint8)).cuda()
     dD = torch.full((128, 256), float("nan"), dtype=torch.float32, device="cuda")
-    rc = rg.lib().moe_testing_mx_tile(dA.data_ptr(), dB.data_ptr(), dI.data_ptr(), dD.data_ptr(), mode,
+    rc = rg.testing_lib().moe_testing_mx_tile(dA.data_ptr(), dB.data_ptr(), dI.data_ptr(), dD.data_ptr(), mode,
                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 0
     torch.cuda.synchronize()

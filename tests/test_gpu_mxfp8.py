@@ -119,18 +119,8 @@ def test_mx_bitwise_deterministic_across_knobs():
         assert np.array_equal(o, outs[0])
 
 
-@pytest.mark.parametrize("dispatch", ["direct", "spread"])
-def test_mx_full_size_dsv3_sampled(dispatch):
-    # spread: the launch configuration the benchmark times
-    inp = mi.make_inputs("dsv3_mxfp8")
-    _, res = run_mx(inp, minibatch=8192, ring_slots=4, dispatch=dispatch)
-    s = inp.shape
-    logits = oracle.router_logits(inp.x, inp.w_router, inp.b_router)
-    idx_ref, g_ref = oracle.topk(logits, s.k, s.score)
-    from test_gpu_parity import compare_routing
-    compare_routing(res, idx_ref, g_ref, s.E)
-    rows = np.unique(np.linspace(0, s.T - 1, 32).astype(np.int64))
-    check_mx(inp, res, rows=rows)
+# Full-size DSV3 MXFP8 (every dispatch mode, CTA pairs, the minibatch sweep):
+# tests/test_gpu_dsv3_full.py.
 
 
 # CTA pairs (mma_pair = 1): one block-scaled tcgen05.mma.cta_group::2 per
@@ -167,15 +157,3 @@ def test_mx_pair_bitwise_deterministic_across_knobs():
         outs.append((kw, res["out"].view(torch.int16).cpu().numpy()))
     for kw, o in outs[1:]:
         assert np.array_equal(o, outs[0][1]), f"output bits differ for {kw}"
-
-
-def test_mx_pair_full_size_dsv3_sampled():
-    inp = mi.make_inputs("dsv3_mxfp8")
-    _, res = run_mx(inp, minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)
-    s = inp.shape
-    logits = oracle.router_logits(inp.x, inp.w_router, inp.b_router)
-    idx_ref, g_ref = oracle.topk(logits, s.k, s.score)
-    from test_gpu_parity import compare_routing
-    compare_routing(res, idx_ref, g_ref, s.E)
-    rows = np.unique(np.linspace(0, s.T - 1, 32).astype(np.int64))
-    check_mx(inp, res, rows=rows)

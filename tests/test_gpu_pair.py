@@ -80,10 +80,6 @@ def test_pair_rejects_unsupported_modes():
             rg.moe_plan_create(256, 256, 128, 16, 4, 128, mma_pair=1, **kw)
 
 
-def test_pair_full_size_dsv3_zipf_sampled():
-    _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)
-
-
 def test_pair_full_size_kimi_k2_sampled():
     # the largest configured shape: T = 32768, E = 384 (uniform load), one shared expert
     _full_size("kimi_k2", minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)

@@ -32,7 +32,7 @@ def run_tile(m, seed=11):
     dA, dB = A.cuda(), B.cuda()
     dD = torch.full((2, 128, 256), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(3, dtype=torch.int32, device="cuda")
-    rc = rg.lib().moe_testing_pair_tile(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), st.data_ptr(), m,
+    rc = rg.testing_lib().moe_testing_pair_tile(dA.data_ptr(), dB.data_ptr(), dD.data_ptr(), st.data_ptr(), m,
                                         torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
@@ -77,7 +77,7 @@ def run_mx_pair(mode, seed=23):
     dA, dB, dS = (torch.from_numpy(v).cuda() for v in (A, B, blocks))
     dD = torch.full((256, 256), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(3, dtype=torch.int32, device="cuda")
-    rc = rg.lib().moe_testing_pair_mx_tile(dA.data_ptr(), dB.data_ptr(), dS.data_ptr(), dD.data_ptr(), st.data_ptr(),
+    rc = rg.testing_lib().moe_testing_pair_mx_tile(dA.data_ptr(), dB.data_ptr(), dS.data_ptr(), dD.data_ptr(), st.data_ptr(),
                                            mode, torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()

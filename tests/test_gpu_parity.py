@@ -155,9 +155,8 @@ def _full_size(name, n_sample=48, **plan_kw):
     return g.check_out(got, ref)
 
 
-@pytest.mark.parametrize("dispatch", ["ring", "direct", "spread"])
-def test_full_size_dsv3_zipf_sampled(dispatch):
-    _full_size("dsv3", minibatch=8192, ring_slots=4, gather_ctas=8, dispatch=dispatch)
+# The DSV3-shaped layer at full size, every dispatch mode and the minibatch
+# sweep: tests/test_gpu_dsv3_full.py (one set of device weights for all).
 
 
 def test_full_size_qwen3_sampled():
