@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 sub-measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the forward + backward measurement")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the minibatch sweep (512 / 2048 / 8192 / 32768 and ring vs over-allocation)")
     ap.add_argument("--gather-ctas-mx", type=int, default=6, help="gather CTAs for the MXFP8 layer")
@@ -526,6 +527,99 @@ def minibatch_sweep(run, steps, warmup):
             "best_over_worst": max(p["tokens_per_s"] for p in out[:4]) / min(p["tokens_per_s"] for p in out[:4])}
 
 
+def backward_flops(shape):
+    """(phase 0, phase 1) FLOPs the backward executes: the replayed up/gate
+    projections and dh' = W_down^T dO (6 T k D I routed, 6 T D I_s shared), then
+    dx (4 T k D I), dW_down (2 T k D I) and dW_up, dW_gate (4 T k D I), and the
+    shared expert's alike.  The pages count the backward as 2x the forward's
+    6 T (k + 1) D I without the replay ("Mixture-of-Kittens", Sec. 4.1)."""
+    R = shape.T * shape.k
+    sh = shape.T * shape.I_s
+    return 6.0 * R * shape.D * shape.I + 6.0 * sh * shape.D, 10.0 * R * shape.D * shape.I + 10.0 * sh * shape.D
+
+
+def backward_timing(run, steps, warmup, bf16_peak, burst_peak, peak_src, sampler=None):
+    """A training step of the layer: moe_fwd then moe_bwd (upstream gradient
+    dO ~ N(0, 1), seeded), every gradient written.  Events bracket the
+    forward's and the backward's phases."""
+    torch, rg, shape = run.torch, run.rg, run.shape
+    T = shape.T
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    dO = dev(mi.grad_out(shape))
+    bf = torch.bfloat16
+    g = {"dx": torch.empty((T, shape.D), dtype=bf, device="cuda"),
+         "dW_router": torch.empty((shape.E, shape.D), dtype=torch.float32, device="cuda"),
+         "db_router": torch.empty(shape.E, dtype=torch.float32, device="cuda") if run.inp.b_router is not None
+         else None,
+         "dW_up": torch.empty((shape.E, shape.I, shape.D), dtype=bf, device="cuda"),
+         "dW_gate": torch.empty((shape.E, shape.I, shape.D), dtype=bf, device="cuda"),
+         "dW_down": torch.empty((shape.E, shape.D, shape.I), dtype=bf, device="cuda")}
+    if shape.I_s:
+        g.update(dWs_up=torch.empty((shape.I_s, shape.D), dtype=bf, device="cuda"),
+                 dWs_gate=torch.empty((shape.I_s, shape.D), dtype=bf, device="cuda"),
+                 dWs_down=torch.empty((shape.D, shape.I_s), dtype=bf, device="cuda"))
+    wsb = rg.moe_bwd_workspace_bytes(run.plan, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+
+    def step():
+        run.step()
+        rg.moe_bwd(run.plan, T, run.x, run.w, dO, run.ws, g, ws, wsb, stream=run.stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if rg.moe_get_status(run.plan, ws, stream=run.stream) != 0:
+        raise SystemExit("backward: device status after warm-up")
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for e in [x for ev in fev + bev for x in ev]:
+        e.record(run.stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    start.record(run.stream)
+    for i in range(steps):
+        rg.moe_plan_set_timing_events(run.plan, fev[i])
+        rg.moe_plan_set_bwd_timing_events(run.plan, bev[i])
+        step()
+    end.record(run.stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    rg.moe_plan_set_timing_events(run.plan, None)
+    rg.moe_plan_set_bwd_timing_events(run.plan, None)
+    if rg.moe_get_status(run.plan, ws, stream=run.stream) != 0:
+        raise SystemExit("backward: device status in the timed region")
+    el = start.elapsed_time(end)
+    mean = lambda xs: sum(xs) / len(xs)
+    ph = {"gather": mean([b[0].elapsed_time(b[1]) for b in bev]),
+          "replay_and_activation_grad_gemm": mean([b[1].elapsed_time(b[2]) for b in bev]),
+          "input_and_weight_grad_gemm": mean([b[2].elapsed_time(b[3]) for b in bev]),
+          "router_and_dx_combine": mean([b[3].elapsed_time(b[4]) for b in bev])}
+    bwd_ms = mean([b[0].elapsed_time(b[4]) for b in bev])
+    fwd_ms = mean([f[0].elapsed_time(f[3]) for f in fev])
+    f0, f1 = backward_flops(shape)
+    fl_fwd = shape.flops()
+    roof = {}
+    for name, fl, ms in (("bwd_gemm_phase0", f0, ph["replay_and_activation_grad_gemm"]),
+                         ("bwd_gemm_phase1", f1, ph["input_and_weight_grad_gemm"])):
+        ach = fl / (ms / 1000.0) / 1e12
+        roof[name] = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s",
+                      "frac": ach / bf16_peak, "frac_of_burst_peak": ach / burst_peak,
+                      "flops_per_launch": fl, "ms": ms,
+                      "peak_source": f"{peak_src} bf16 sustained"}
+    del ws, g
+    return {"workload": f"{shape.name}: forward + backward (every gradient), dO ~ N(0, 1) seeded",
+            "fwd_bwd_tokens_per_s": T * steps / (el / 1000.0), "ms_per_step": el / steps,
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_phases_ms": ph,
+            "bwd_tflops_pages_convention": 2.0 * fl_fwd / (bwd_ms / 1000.0) / 1e12,
+            "bwd_tflops_executed": (f0 + f1) / (bwd_ms / 1000.0) / 1e12,
+            "bwd_flops_note": "pages: backward = 2x the forward's 6T(k+1)DI; executed adds the replayed "
+                              "up/gate projections (16 T k D I + 16 T D I_s in all)",
+            "roofline": roof, "gpu_launches_per_step": run.launches + 8, "clocks": clocks}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import routing_grouped_expert_gemm_gb300 as rg
@@ -595,6 +689,9 @@ def run_ours(args, world, rank, local):
                        "serial_value": replica_throughput(world, T, args.steps, e2e_serial["ms"])}
     sweep_steps = max(3, args.steps // 4)
     full_size = not (args.tokens or args.experts)
+    if not args.no_backward and shape.precision == "bf16":
+        line["backward"] = backward_timing(run, max(3, args.steps // 2), 3, bf16_peak, burst_peak, peak_src,
+                                           ClockSampler(local))
     if not args.no_sweep and full_size:
         line["minibatch_sweep"] = minibatch_sweep(run, sweep_steps, 3)
     cpu = None

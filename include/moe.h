@@ -82,7 +82,7 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              ring of minibatches (the pages' communication SMs);
  *              MOE_DISPATCH_DIRECT: the GEMM CTAs' TMA producers fetch each
  *              tile's token rows straight from x (tile::gather4), no gather
- *              CTAs and no x ring (MXFP8: x is quantised once per token first);
+ *              CTAs and no x ring (MXFP8: from the router pass's x codes);
  *              MOE_DISPATCH_SPREAD: the same ring as MOE_DISPATCH_RING, filled
  *              by two otherwise idle warps of every GEMM CTA (each takes the
  *              minibatch's M-tiles c, c + gemm CTAs, ...), so every SM runs
@@ -234,10 +234,9 @@ size_t moe_mxfp8_scale_bytes(int64_t rows, int64_t K);
  *   o          outputs, see moe_outputs
  *   workspace  device memory of at least moe_workspace_bytes(plan, T) bytes,
  *              256-byte aligned; its contents need no initialisation
- * Launches, in order on `stream`: router + top-k, schedule, persistent
- * forward kernel (three kernels; MXFP8 with direct dispatch adds a per-token
- * x quantisation pass before the persistent kernel, ring and spread dispatch
- * quantise x rows on their way into the ring); no host synchronisation.  Two calls on identical
+ * Launches, in order on `stream`: router + top-k (for MXFP8 it also
+ * quantises x per token), schedule, persistent forward kernel -- three
+ * kernels, no host synchronisation.  Two calls on identical
  * inputs give bitwise-identical outputs, also across minibatch, ring_slots,
  * gather_ctas, gemm_ctas and lag settings.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA.
@@ -305,6 +304,70 @@ int moe_route_static(const moe_plan* plan, int64_t T, const void* x, const void*
                      int32_t* topk_idx, float* topk_w, int32_t* expert_counts, int32_t* expert_offsets,
                      int32_t* sched, int32_t* route_row, int32_t* device_status, moe_stream_t stream);
 size_t moe_route_static_scratch_bytes(void);
+
+/*
+ * Gradients of the layer (device pointers), written by moe_bwd.
+ *   dx        [T, D] bf16: dL/dx (required)
+ *   dW_router [E, D] fp32: dL/dW_r (required)
+ *   db_router [E] fp32: dL/db, or NULL (not exported)
+ *   dW_up, dW_gate [E, I, D] bf16; dW_down [E, D, I] bf16 (required)
+ *   dWs_up, dWs_gate [I_s, D] bf16; dWs_down [D, I_s] bf16: the shared
+ *   expert's, required when the forward had a shared expert, else NULL
+ */
+typedef struct moe_grads {
+  void* dx;
+  float* dW_router;
+  float* db_router;
+  void* dW_up;
+  void* dW_gate;
+  void* dW_down;
+  void* dWs_up;
+  void* dWs_gate;
+  void* dWs_down;
+} moe_grads;
+
+/* Bytes of device workspace moe_bwd needs for T tokens (0 on bad input or a
+ * shape the backward does not support: I and I_s must be multiples of 256). */
+size_t moe_bwd_workspace_bytes(const moe_plan* plan, int64_t T);
+
+/*
+ * The backward pass ("Mixture-of-Kittens: MoE Megakernel for NVL72s",
+ * Sec. 3.3 "Ring-Aware Forward Replay" and Sec. 3.4 "Router Weight Gradient
+ * Computation"): given dO = dL/d out for the forward that moe_fwd computed on
+ * the same x and weights with `fwd_workspace` (its routing and schedule are
+ * reused, unmodified, from that workspace), writes every gradient of
+ * moe_grads by the chain rule on Eq. MoE:
+ *   dy_j = g_j dO;  dg_j = <W_down[e]^T dO, h>  (the SonicMoE form: the
+ *   expert output is never materialised);  dh = g_j W_down[e]^T dO;
+ *   da_u = dh * SiLU(a_g);  da_g = dh * a_u * SiLU'(a_g);
+ *   dW_down[e] = sum dy h^T;  dW_up[e] = sum da_u x^T;  dW_gate[e] = sum da_g x^T;
+ *   dx = sum_j (W_up[e]^T da_u + W_gate[e]^T da_g) + shared expert + W_r^T dl,
+ *   with dl from g = s_sel / sum s_sel through the score function.
+ * The gated activations are recomputed (the forward replay): every route's
+ * up/gate projections run again from the gathered x rows.  BF16 routed
+ * experts only (MOE_ERR_UNSUPPORTED_SHAPE for an MXFP8 plan).  No
+ * floating-point atomics: every gradient element is produced by one tile with
+ * a fixed K order or by a fixed-order sum, so two calls give the same bits.
+ *   dO         [T, D] bf16 (device)
+ *   workspace  at least moe_bwd_workspace_bytes(plan, T) bytes, 256-byte aligned
+ * Launches eight kernels on `stream`; no host synchronisation; device-side
+ * failures are reported through moe_get_status on `workspace`.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA.
+ */
+int moe_bwd(const moe_plan* plan, int64_t T, const void* x, const moe_weights* w, const void* dO,
+            const void* fwd_workspace, const moe_grads* grads, void* workspace, size_t workspace_bytes,
+            moe_stream_t stream);
+
+/*
+ * Optional per-phase timing of moe_bwd for profiling harnesses: with events
+ * != NULL, every later moe_bwd with this plan records events[0] before its
+ * first launch, events[1] after the gather of the routes' x and dO rows,
+ * events[2] after the replay + activation-gradient GEMMs, events[3] after the
+ * input- and weight-gradient GEMMs and events[4] after its last launch;
+ * NULL turns it off.  The caller owns the events (cudaEvent_t).
+ */
+int moe_plan_set_bwd_timing_events(moe_plan* plan, void* const* events);
 
 /* Static description of an error code. */
 const char* moe_error_string(int code);

@@ -64,6 +64,19 @@ int moe_testing_pair_mma_time(const void* A, const void* B, float* D, int* statu
 int moe_testing_pair_mx_tile(const void* A, const void* B, const void* sf, float* D, int* status, int mode,
                              void* stream);
 
+/*
+ * One bf16 tcgen05 MMA tile with operands staged K-major or MN-major:
+ *   D [128, N] fp32 = A [128, 64] B [N, 64]^T,  N = 128 or 256,
+ * A and B row-major bf16 (K contiguous) in device memory.  a_mn / b_mn = 1
+ * stage that operand MN-major in shared memory (64-wide MN blocks of 64 K rows
+ * x 128 B, 128-byte swizzle, 8192 B apart) and set its major bit in the
+ * instruction descriptor; its matrix descriptor gets leading byte offset lbo
+ * and stride byte offset sbo, (lbo, sbo) = (8192, 1024) or (1024, 8192).
+ * Asynchronous on `stream`.  Returns 0, -1 (bad argument) or -4 (CUDA error).
+ */
+int moe_testing_mn_tile(const void* A, const void* B, float* D, int N, int a_mn, int b_mn, int lbo, int sbo,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

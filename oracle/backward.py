@@ -106,17 +106,29 @@ def moe_fwd(p: dict, k: int, score: str) -> dict:
             "shared": shared}
 
 
-def moe_bwd(p: dict, k: int, score: str, dO: np.ndarray) -> dict:
+def moe_bwd(p: dict, k: int, score: str, dO: np.ndarray, experts=None) -> dict:
     """dL/d(inputs) for L with dL/d out = dO, as listed in the module docstring.
     Keys: x, w_router, b_router, w_up, w_gate, w_down, ws_up, ws_gate, ws_down
-    (None where the input is None)."""
+    (None where the input is None).
+
+    ``experts``: None, or a list of expert ids whose weight gradients are
+    wanted; then w_up / w_gate / w_down only need ``.shape`` and ``[e]``
+    (an object that converts one expert at a time will do) and the routed
+    weight gradients are returned as {e: array} for those experts only.  The
+    arithmetic is the same either way."""
     f = moe_fwd(p, k, score)
     x = p["x"]
     T, D = x.shape
     E = p["w_router"].shape[0]
     idx, g, s, S = f["idx"], f["g"], f["s"], f["S"]
     dx = np.zeros_like(x)
-    dw_up, dw_gate, dw_down = np.zeros_like(p["w_up"]), np.zeros_like(p["w_gate"]), np.zeros_like(p["w_down"])
+    if experts is None:
+        dw_up, dw_gate, dw_down = np.zeros_like(p["w_up"]), np.zeros_like(p["w_gate"]), np.zeros_like(p["w_down"])
+    else:
+        I = p["w_up"].shape[1]
+        dw_up = {e: np.zeros((I, D)) for e in experts}
+        dw_gate = {e: np.zeros((I, D)) for e in experts}
+        dw_down = {e: np.zeros((D, I)) for e in experts}
     dg = np.zeros((T, k))
     for e in range(E):
         tt, jj = np.nonzero(idx == e)
@@ -125,14 +137,16 @@ def moe_bwd(p: dict, k: int, score: str, dO: np.ndarray) -> dict:
         au, ag = f["a_u"][tt, jj], f["a_g"][tt, jj]
         h = _silu(ag) * au
         dOe = dO[tt]
-        dg[tt, jj] = np.einsum("nd,nd->n", dOe @ p["w_down"][e], h)  # <W_down^T dO, h>
+        wdn = p["w_down"][e]
+        dg[tt, jj] = np.einsum("nd,nd->n", dOe @ wdn, h)  # <W_down^T dO, h>
         dy = g[tt, jj][:, None] * dOe
-        dh = dy @ p["w_down"][e]
-        dw_down[e] += dy.T @ h
+        dh = dy @ wdn
         da_u = dh * _silu(ag)
         da_g = dh * au * _dsilu(ag)
-        dw_up[e] += da_u.T @ x[tt]
-        dw_gate[e] += da_g.T @ x[tt]
+        if experts is None or e in dw_up:
+            dw_down[e] += dy.T @ h
+            dw_up[e] += da_u.T @ x[tt]
+            dw_gate[e] += da_g.T @ x[tt]
         np.add.at(dx, tt, da_u @ p["w_up"][e] + da_g @ p["w_gate"][e])
     # router: g = s_sel / S
     c = np.einsum("tj,tj->t", g, dg)

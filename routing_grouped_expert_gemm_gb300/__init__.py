@@ -7,7 +7,8 @@ used only to hand over device pointers and streams.
 
 Entry points keep the C names: ``moe_plan_create``, ``moe_plan_destroy``,
 ``moe_workspace_bytes``, ``moe_quantize_mxfp8``, ``moe_mxfp8_scale_bytes``,
-``moe_fwd``, ``moe_get_status``, ``moe_error_string``.
+``moe_fwd``, ``moe_bwd_workspace_bytes``, ``moe_bwd``, ``moe_get_status``,
+``moe_get_phase_times``, ``moe_route_static``, ``moe_error_string``.
 """
 from __future__ import annotations
 
@@ -62,6 +63,11 @@ class moe_weights(ctypes.Structure):
         "Ws_up", "Ws_gate", "Ws_down")]
 
 
+class moe_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "dx", "dW_router", "db_router", "dW_up", "dW_gate", "dW_down", "dWs_up", "dWs_gate", "dWs_down")]
+
+
 class moe_outputs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "out", "topk_idx", "topk_w", "expert_counts", "expert_offsets", "sched", "route_row")]
@@ -95,6 +101,12 @@ def lib():
     L.moe_get_status.restype = ctypes.c_int
     L.moe_plan_set_timing_events.argtypes = [vp, ctypes.POINTER(vp)]
     L.moe_plan_set_timing_events.restype = ctypes.c_int
+    L.moe_plan_set_bwd_timing_events.argtypes = [vp, ctypes.POINTER(vp)]
+    L.moe_plan_set_bwd_timing_events.restype = ctypes.c_int
+    L.moe_bwd_workspace_bytes.argtypes = [vp, i64]
+    L.moe_bwd_workspace_bytes.restype = sz
+    L.moe_bwd.argtypes = [vp, i64, vp, ctypes.POINTER(moe_weights), vp, vp, ctypes.POINTER(moe_grads), vp, sz, vp]
+    L.moe_bwd.restype = ctypes.c_int
     L.moe_get_phase_times.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double), vp]
     L.moe_get_phase_times.restype = ctypes.c_int
     L.moe_route_static.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -127,6 +139,9 @@ def testing_lib():
     L.moe_testing_pair_mma_time.restype = ctypes.c_int
     L.moe_testing_pair_mx_tile.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, vp]
     L.moe_testing_pair_mx_tile.restype = ctypes.c_int
+    L.moe_testing_mn_tile.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, vp]
+    L.moe_testing_mn_tile.restype = ctypes.c_int
     _testing_lib = L
     return L
 
@@ -224,6 +239,25 @@ def moe_fwd(plan: Plan, T: int, x, weights: dict, out, workspace, workspace_byte
         raise MoEError(rc, "moe_fwd")
 
 
+def moe_bwd_workspace_bytes(plan: Plan, T: int) -> int:
+    return int(lib().moe_bwd_workspace_bytes(plan.handle, T))
+
+
+def moe_bwd(plan: Plan, T: int, x, weights: dict, dO, fwd_workspace, grads: dict, workspace,
+            workspace_bytes: int | None = None, stream=None) -> None:
+    """Backward pass: ``grads`` has keys of moe_grads (dx, dW_router, db_router,
+    dW_up, dW_gate, dW_down, dWs_up, dWs_gate, dWs_down); ``fwd_workspace`` is
+    the workspace of the moe_fwd call on the same x and weights."""
+    w = moe_weights(**{k: _ptr(v) for k, v in weights.items()})
+    g = moe_grads(**{k: _ptr(v) for k, v in grads.items()})
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().moe_bwd(plan.handle, T, _ptr(x), ctypes.byref(w), _ptr(dO), _ptr(fwd_workspace), ctypes.byref(g),
+                       _ptr(workspace), workspace_bytes, _stream(stream))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_bwd")
+
+
 def moe_get_status(plan: Plan, workspace, stream=None) -> int:
     st = ctypes.c_int(-1)
     rc = lib().moe_get_status(plan.handle, _ptr(workspace), ctypes.byref(st), _stream(stream))
@@ -252,6 +286,17 @@ def moe_plan_set_timing_events(plan: Plan, events) -> None:
         rc = lib().moe_plan_set_timing_events(plan.handle, arr)
     if rc != MOE_OK:
         raise MoEError(rc, "moe_plan_set_timing_events")
+
+
+def moe_plan_set_bwd_timing_events(plan: Plan, events) -> None:
+    """events: five torch.cuda.Event (created with enable_timing) or None."""
+    if events is None:
+        rc = lib().moe_plan_set_bwd_timing_events(plan.handle, None)
+    else:
+        arr = (ctypes.c_void_p * 5)(*[int(e.cuda_event) for e in events])
+        rc = lib().moe_plan_set_bwd_timing_events(plan.handle, arr)
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_plan_set_bwd_timing_events")
 
 
 def moe_route_static(plan: Plan, T: int, x, W_router, b_router, topk_idx, topk_w, expert_counts, expert_offsets,

@@ -18,7 +18,6 @@ cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int gr
 int megakernel_smem_bytes();
 int megakernel_pair_max_ctas(bool mx);
 cudaError_t launch_mx_quantize(const bf16* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
-cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st);
 size_t mx_scale_bytes(int64_t rows, int64_t K);
 }  // namespace moe
 
@@ -31,7 +30,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Layout {
-  size_t status, counters, meta, topk_idx, topk_w, chunk_counts, M, S, sched, route_row, mtiles, segs, tasks;
+  size_t status, counters, meta, topk_idx, topk_w, topk_logit, chunk_counts, M, S, sched, route_row, mtiles, segs, tasks;
   size_t ring_x, ring_h, sfx, sfh, xq, xs, h_s, Y, trace, total;
   int64_t n_mb, n_mtiles_max, n_smtiles, n_tasks_max, n_counters, n_chunks, max_segs, R;
 };
@@ -61,6 +60,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.meta = take(sizeof(int) * (META_MB + 4 * L.n_mb));
   L.topk_idx = take(sizeof(int) * L.R);
   L.topk_w = take(sizeof(float) * L.R);
+  L.topk_logit = take(sizeof(float) * L.R);
   L.chunk_counts = take(sizeof(int) * L.n_chunks * c.E);
   L.M = take(sizeof(int) * c.E);
   L.S = take(sizeof(int) * (c.E + 1));
@@ -76,10 +76,9 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   L.ring_x = take(direct ? 0 : (size_t)ring_rows * c.D * elem);
   L.ring_h = take((size_t)ring_rows * c.I * elem);
   L.sfx = take(mx && !direct ? (size_t)L.n_mtiles_max * (c.D / BK_MX) * SF_BLOCK_BYTES : 0);
-  // direct dispatch: x quantised once per token before the persistent kernel
-  // (ring and spread dispatch quantise the rows on their way into the ring)
-  L.xq = take(mx && direct ? (size_t)T * c.D : 0);
-  L.xs = take(mx && direct ? (size_t)T * (c.D / 32) : 0);
+  // MXFP8: x quantised once per token by the router pass (it reads every row)
+  L.xq = take(mx ? (size_t)T * c.D : 0);
+  L.xs = take(mx ? (size_t)T * (c.D / 32) : 0);
   L.sfh = take(mx ? (size_t)L.n_mtiles_max * (c.I / BK_MX) * SF_BLOCK_BYTES : 0);
   L.h_s = take((size_t)T * c.I_s * 2);
   L.Y = take((size_t)L.n_chunks * BM * (c.k + (c.I_s > 0 ? 1 : 0)) * c.D * 2);  // blocked by token tile, see FwdParams::Y
@@ -129,6 +128,23 @@ int encode_sf_blocks(const moe_plan* pl, CUtensorMap* m, const void* ptr, size_t
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace moe {
+// Where a forward of T tokens keeps its routing and schedule in its workspace
+// (read by the backward pass, which reuses them).
+int fwd_routing_views(const moe_plan* pl, int64_t T, const void* workspace, FwdRoutingViews* v) {
+  if (!pl || !workspace || !v || T < 1 || T > pl->cfg.T_max) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(pl, T);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  v->topk_idx = reinterpret_cast<const int*>(ws + L.topk_idx);
+  v->topk_w = reinterpret_cast<const float*>(ws + L.topk_w);
+  v->topk_logit = reinterpret_cast<const float*>(ws + L.topk_logit);
+  v->M = reinterpret_cast<const int*>(ws + L.M);
+  v->S = reinterpret_cast<const int*>(ws + L.S);
+  v->sched = reinterpret_cast<const int*>(ws + L.sched);
+  return MOE_OK;
+}
+}  // namespace moe
 
 extern "C" {
 
@@ -210,6 +226,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   pl->grid = c.gather_ctas + gemm;
   pl->encode = reinterpret_cast<encode_tiled_fn>(fn);
   pl->timed = false;
+  pl->bwd_timed = false;
   *out = pl;
   return MOE_OK;
 }
@@ -242,6 +259,20 @@ int moe_get_phase_times(const moe_plan* plan, const void* workspace, double* tim
   times_ms[0] = rel(st[STAMP_LAST_FILL]);
   times_ms[1] = rel(st[STAMP_COMBINE_START]);
   times_ms[2] = rel(st[STAMP_COMBINE_END]);
+  return MOE_OK;
+}
+
+int moe_plan_set_bwd_timing_events(moe_plan* plan, void* const* events) {
+  if (!plan) return MOE_ERR_INVALID_ARG;
+  if (!events) {
+    plan->bwd_timed = false;
+    return MOE_OK;
+  }
+  for (int i = 0; i < 5; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+    plan->bwd_timing[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  plan->bwd_timed = true;
   return MOE_OK;
 }
 
@@ -335,6 +366,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.meta = reinterpret_cast<int*>(ws + L.meta);
   p.topk_idx = reinterpret_cast<int*>(ws + L.topk_idx);
   p.topk_w = reinterpret_cast<float*>(ws + L.topk_w);
+  p.topk_logit = reinterpret_cast<float*>(ws + L.topk_logit);
   p.chunk_counts = reinterpret_cast<int*>(ws + L.chunk_counts);
   p.M = reinterpret_cast<int*>(ws + L.M);
   p.S = reinterpret_cast<int*>(ws + L.S);
@@ -345,8 +377,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.tasks = reinterpret_cast<Task*>(ws + L.tasks);
   p.ring_x = reinterpret_cast<bf16*>(ws + L.ring_x);
   p.ring_h = reinterpret_cast<bf16*>(ws + L.ring_h);
-  p.xq = mx && p.direct ? ws + L.xq : nullptr;
-  p.xs = mx && p.direct ? ws + L.xs : nullptr;
+  p.xq = mx ? ws + L.xq : nullptr;
+  p.xs = mx ? ws + L.xs : nullptr;
   p.sfx = mx && !p.direct ? ws + L.sfx : nullptr;
   p.sfh = mx ? ws + L.sfh : nullptr;
   p.w_up_sf = mx ? w->W_up_scale : nullptr;
@@ -416,8 +448,6 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   if (pl->timed && cudaEventRecord(pl->timing[1], stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_schedule(p, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[2], stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (mx && p.direct && launch_mx_quantize_rows(p.x, p.T, p.D, p.xq, p.xs, stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
   if (launch_megakernel(tm, p, pl->grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (pl->timed && cudaEventRecord(pl->timing[3], stream) != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -117,6 +117,7 @@ struct FwdParams {
   int* meta;
   int* topk_idx;      // [T,k]
   float* topk_w;      // [T,k]
+  float* topk_logit;  // [T,k] the selected experts' biased fp32 logits (kept for the backward pass), or null
   int* chunk_counts;  // [n_chunks, E]
   int* M;             // [E]
   int* S;             // [E+1]

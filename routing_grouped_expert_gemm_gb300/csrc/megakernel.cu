@@ -79,40 +79,32 @@ __device__ void gather_copy_row(const FwdParams& p, const bf16* src_row, bf16* d
   }
 }
 
-// MXFP8: token t's bf16 row quantised on the way into the ring (OCP MX,
-// E4M3 codes + one E8M0 scale per 32 elements along D, the same rule as the
-// weight quantiser): lane l takes the 32-element blocks l, l + 32, ...; its
-// codes go to the ring row, and the four scales of each 128-wide K step (four
-// neighbouring lanes) as one 32-bit word into the M-tile's scale block at row
-// r_in_tile.  D / 32 is a multiple of 8, so every K step's four blocks sit in
-// lanes 4q .. 4q + 3 of one pass.
-__device__ void gather_quant_row_mx(const FwdParams& p, int t, uint8_t* dst_row, uint8_t* sf_tile, int r_in_tile) {
+// MXFP8: a token's E4M3 codes into a ring row (the warp's lanes copy 16-byte
+// vectors, the whole row in flight) and its E8M0 words into the M-tile's
+// scale blocks (one word per 128-wide K step, row r_in_tile of the tile)
+__device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, uint8_t* sf_tile, int r_in_tile) {
   const int lane = threadIdx.x & 31;
-  const int nblk = p.D / 32;
-  const bf16* src = p.x + (size_t)t * p.D;
-#pragma unroll 2
-  for (int b0 = 0; b0 < nblk; b0 += 32) {
-    const int b = b0 + lane;
-    uint32_t sc = 0;
-    if (b < nblk) {
-      float v[32];
-      load_bf16x32(src + (size_t)b * 32, v);
-      uint32_t q[8];
-      sc = mx_quantize32(v, q);
-      uint4* d = reinterpret_cast<uint4*>(dst_row + (size_t)b * 32);
-      d[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  const int nv = p.D / 16;
+  constexpr int UNR = 16;  // D <= 8192 in one pass
+  const uint4* src = reinterpret_cast<const uint4*>(p.xq + (size_t)t * p.D);
+  uint4* dst = reinterpret_cast<uint4*>(dst_row);
+  for (int base = 0; base < nv; base += 32 * UNR) {
+    uint4 v[UNR];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) v[u] = __ldg(src + i);
     }
-    // lanes 4q .. 4q + 3 hold K step (b0 + 4q) / 4's four scales
-    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sc, 1);
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sc, 2);
-    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sc, 3);
-    if ((lane & 3) == 0 && b < nblk) {
-      const int kg = b >> 2;
-      *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) =
-          sc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int i = base + u * 32 + lane;
+      if (i < nv) dst[i] = v[u];
     }
   }
+  const int nkg = p.D / BK_MX;
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.xs + (size_t)t * (p.D / 32));
+  for (int kg = lane; kg < nkg; kg += 32)
+    *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r_in_tile, 0)) = __ldg(sw + kg);
 }
 
 // Ring fill spread over the GEMM CTAs (MOE_DISPATCH_SPREAD): warps 6 and 7
@@ -141,8 +133,8 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
         const int t = p.sched[(size_t)(p0 + r) * 3];
         const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
         if (p.mx)
-          gather_quant_row_mx(p, t, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
-                              p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
+          gather_copy_row_mx(p, t, reinterpret_cast<uint8_t*>(p.ring_x) + ring_row * p.D,
+                             p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES, r);
         else
           gather_copy_row(p, p.x + (size_t)t * p.D, p.ring_x + ring_row * p.D);
       }
@@ -224,8 +216,9 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* b
   TRACE_LOCALS();
   const int g = blockIdx.x;
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t row_bytes = (uint32_t)p.D * 2u;  // a bf16 ring row (the bulk path)
-  const uint8_t* src = reinterpret_cast<const uint8_t*>(p.x);
+  // a ring row: D bf16, or D E4M3 codes
+  const uint32_t row_bytes = (uint32_t)p.D * (p.mx ? 1u : 2u);
+  const uint8_t* src = p.mx ? p.xq : reinterpret_cast<const uint8_t*>(p.x);
   uint8_t* dst = reinterpret_cast<uint8_t*>(p.ring_x);
   const int nbuf = min(GATHER_BUFS, buf_bytes / (int)row_bytes);  // >= 12 for D <= 8192
   uint32_t row_seq = 0;
@@ -249,27 +242,13 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* b
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
     TRACE_T0();
-    if (p.mx) {
-      // MXFP8: every warp quantises whole token rows on the way in (codes to
-      // the ring, scale words to the tile's scale blocks); this CTA takes the
-      // minibatch's M-tiles g, g + G, ...
-      const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
-      for (int i = g; i < ntile; i += p.G) {
-        const int mt = mt0 + i;
-        const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
-        uint8_t* sf_tile = p.sfx + (size_t)mt * (p.D / BK_MX) * SF_BLOCK_BYTES;
-        for (int r = warp; r < rows; r += nwarps) {
-          const int t = p.sched[(size_t)(p0 + r) * 3];
-          gather_quant_row_mx(p, t, dst + (slot_base + (size_t)(p0 + r - lo)) * p.D, sf_tile, r);
-        }
-      }
-    } else if (warp == 0) {
-      // contiguous row ranges per CTA; the rows' tokens go to a shared table
-      // first (32 lanes, independent loads), so the issuing lane never waits
-      // on a global load per row
-      const int hi = min(p.R, lo + p.b);
-      const int per = (hi - lo + p.G - 1) / p.G;
-      const int r0 = lo + g * per, r1 = min(hi, r0 + per);
+    // contiguous row ranges per CTA for the rows themselves
+    const int hi = min(p.R, lo + p.b);
+    const int per = (hi - lo + p.G - 1) / p.G;
+    const int r0 = lo + g * per, r1 = min(hi, r0 + per);
+    if (warp == 0) {
+      // the rows' tokens go to a shared table first (32 lanes, independent
+      // loads), so the issuing lane never waits on a global load per row
       bool ok = true;
       for (int c0 = r0; c0 < r1 && ok; c0 += GATHER_TOK_CHUNK) {
         const int c1 = min(r1, c0 + GATHER_TOK_CHUNK);
@@ -283,6 +262,23 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* b
         __syncwarp();
       }
       if (lane == 0 && !ok) *s_flag = 0;
+    } else if (p.mx) {
+      // MXFP8: the other warps put the tokens' E8M0 words into the scale
+      // blocks of the minibatch's M-tiles g, g + G, ... (one word per row and
+      // 128-wide K step)
+      const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
+      const int nkg = p.D / BK_MX;
+      for (int i = g; i < ntile; i += p.G) {
+        const int mt = mt0 + i;
+        const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
+        uint8_t* sf_tile = p.sfx + (size_t)mt * nkg * SF_BLOCK_BYTES;
+        for (int r = warp - 1; r < rows; r += nwarps - 1) {
+          const int t = p.sched[(size_t)(p0 + r) * 3];
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(p.xs + (size_t)t * (p.D / 32));
+          for (int kg = lane; kg < nkg; kg += 32)
+            *reinterpret_cast<uint32_t*>(sf_tile + (size_t)kg * SF_BLOCK_BYTES + sf_offset(r, 0)) = __ldg(sw + kg);
+        }
+      }
     }
     fence_proxy_async_global();
     __syncthreads();

@@ -65,36 +65,6 @@ __global__ void mx_quantize_kernel(const bf16* __restrict__ W, int64_t rows, int
   }
 }
 
-// Activation quantisation for direct dispatch (Sec. 3.4: activation
-// quantisation is fused into the dispatch): every token row of x is quantised
-// once, whatever the number of experts it goes to.  One warp per row, lane l
-// takes the 32-element blocks l, l + 32, ...; codes [T, D], scales [T, D/32].
-__global__ void __launch_bounds__(256) mx_quantize_rows_kernel(const bf16* __restrict__ x, int T, int D,
-                                                                uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
-  const int lane = threadIdx.x & 31;
-  const int nblk = D / 32;
-  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += gridDim.x * (blockDim.x >> 5)) {
-#pragma unroll 2
-    for (int blk = lane; blk < nblk; blk += 32) {
-      float v[32];
-      load_bf16x32(x + (size_t)t * D + blk * 32, v);
-      uint32_t q[8];
-      const uint32_t code = mx_quantize32(v, q);
-      uint4* dst = reinterpret_cast<uint4*>(xq + (size_t)t * D + blk * 32);
-      dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      xs[(size_t)t * nblk + blk] = (uint8_t)code;
-    }
-  }
-}
-
-cudaError_t launch_mx_quantize_rows(const bf16* x, int T, int D, uint8_t* xq, uint8_t* xs, cudaStream_t st) {
-  int grid = (T + 7) / 8;
-  if (grid > 152 * 8) grid = 152 * 8;
-  mx_quantize_rows_kernel<<<grid, 256, 0, st>>>(x, T, D, xq, xs);
-  return cudaGetLastError();
-}
-
 size_t mx_scale_bytes(int64_t rows, int64_t K) { return (size_t)(rows * (K / 32)); }
 
 cudaError_t launch_mx_quantize(const bf16* W, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st) {

@@ -11,6 +11,15 @@
 //
 // The kernel also zeroes the persistent kernel's counters and the status word
 // and writes each CTA's per-expert route histogram (input of the schedule).
+//
+// MXFP8 routed experts (Sec. 3.4 "MXFP8 Support": activation quantisation
+// fused into the dispatch): this is the one pass that reads every token's x
+// row, so it also quantises x for the expert GEMMs.  While the MMA consumes a
+// stage, the four epilogue warps (idle until the logits are ready) read the
+// same x tile from shared memory, one row per thread, and write its E4M3 codes
+// and E8M0 scales (OCP MX, 32-element blocks along D) to the workspace; the
+// stage is refilled only after the MMA and the four warps have released it.
+// The dispatch then moves the codes into the ring.
 #include "common.cuh"
 
 namespace moe {
@@ -34,6 +43,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS, 1)
   const int stage_bytes = A_STAGE_BYTES + ncols * 128;
   uint64_t* full = s_bar;
   uint64_t* empty = s_bar + 8;
+  const bool quant = p.mx && p.xq != nullptr;  // MXFP8: the epilogue warps quantise x on the way
   uint64_t* tfull = s_bar + 16;
   uint64_t* drain = s_bar + 17;
 
@@ -58,7 +68,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], quant ? 5 : 1);  // the MMA's commit (+ one arrival per quantising warp)
     }
     mbar_init(tfull, 1);
     mbar_init(drain, 1);
@@ -127,6 +137,39 @@ __global__ void __launch_bounds__(ROUTER_THREADS, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int t = t0 + row;
+    if (quant) {
+      // this thread's row of every x stage: 64 bf16 (one 128-byte swizzled
+      // row, 16-byte chunk c at c ^ (row % 8)) -> two MX blocks of 32
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % stages;
+        if (!mbar_wait(&full[s], (uint32_t)(kb / stages) & 1u, p.status, p.timeout_ns)) break;
+        const uint8_t* a = smem + s * stage_bytes + row * 128;
+        float v[64];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(a + ((c ^ (row & 7)) << 4));
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            v[8 * c + 2 * j] = f.x;
+            v[8 * c + 2 * j + 1] = f.y;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // the stage's x tile is read
+        uint32_t c0[8], c1[8];
+        const uint32_t s0 = mx_quantize32(v, c0), s1 = mx_quantize32(v + 32, c1);
+        if (t < p.T) {
+          uint4* d = reinterpret_cast<uint4*>(p.xq + (size_t)t * p.D + kb * BK);
+          d[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+          d[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
+          d[2] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+          d[3] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+          *reinterpret_cast<uint16_t*>(p.xs + (size_t)t * (p.D / 32) + 2 * kb) = (uint16_t)(s0 | (s1 << 8));
+        }
+      }
+    }
     if (mbar_wait(tfull, 0, p.status, p.timeout_ns)) {
       tc_fence_after();
       float bv[TOPK_MAX];
@@ -202,6 +245,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS, 1)
           if (i < k) {
             p.topk_idx[(size_t)t * k + i] = bi[i];
             p.topk_w[(size_t)t * k + i] = s[i] * inv;
+            if (p.topk_logit) p.topk_logit[(size_t)t * k + i] = bv[i];
             atomicAdd(&s_hist[bi[i]], 1);
           }
         }

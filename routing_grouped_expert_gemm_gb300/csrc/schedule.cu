@@ -7,9 +7,9 @@
 // route j (= t*k + slot) lands at S_l + o, o being the number of earlier
 // routes to the same expert.  Table row P holds {src_index = t, expert = l,
 // dst_index = j}: the gather reads x[t] into ring position P, and the combine
-// reuses the table the other way round, writing expert output row P to the
-// token-order staging row j (Sec. 3.1, "Finally, the schedule can be built
-// once and reused").
+// reads the same table the other way round, writing expert output row P to the
+// token-order staging row j (Sec. 3.1: one table, built once, serves the
+// dispatch, the combine and the backward pass's counterparts).
 //
 // One CTA per 128-token chunk (the router's tiles): each CTA sums the router's
 // per-chunk histograms (its own prefix and the totals), scans them, and ranks

@@ -18,7 +18,8 @@ def L():
 
 EXPECTED = {"moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_quantize_mxfp8",
             "moe_mxfp8_scale_bytes", "moe_fwd", "moe_get_status", "moe_error_string",
-            "moe_plan_set_timing_events", "moe_get_phase_times", "moe_route_static", "moe_route_static_scratch_bytes"}
+            "moe_plan_set_timing_events", "moe_get_phase_times", "moe_route_static", "moe_route_static_scratch_bytes",
+            "moe_bwd", "moe_bwd_workspace_bytes", "moe_plan_set_bwd_timing_events"}
 
 
 def test_header_declares_the_boundary():

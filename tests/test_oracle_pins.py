@@ -207,9 +207,9 @@ def test_token_subset_equals_full_run():
 
 # ------------------------------------------------------------------ schedule (Algorithm 1)
 @pytest.mark.parametrize("R,L,N,K,c", [(1, 4, 10, 2, 0), (2, 3, 7, 2, 1), (3, 2, 9, 3, 0), (3, 4, 5, 4, 2)])
-def test_alg1_closed_form_equals_sort_key(R, L, N, K, c):
+def test_alg1_round_robin_merge_equals_sort_key(R, L, N, K, c):
     """Sec. 3.1: the table is the routes sorted by (local expert, ordinal o,
-    source rank r); Algorithm 1's closed-form position must produce exactly it."""
+    source rank r); the count-scan-merge construction must produce exactly it."""
     rnd = random.Random(R * 100 + L * 10 + N)
     for _ in range(20):
         A = []
