@@ -72,6 +72,9 @@ def parse_args():
     ap.add_argument("--gemm-ctas", type=int, default=0, help="CTAs that run expert tiles (0 = all remaining SMs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: a smaller case with this many tokens (uniform routing)")
+    ap.add_argument("--route-only", action="store_true",
+                    help="profiling only: time the routing stage alone (moe_route_static: router + top-k + "
+                         "schedule) on the workload's x and router; no expert weights on the device")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: a smaller case with this many routed experts (uniform routing)")
     return ap.parse_args()
@@ -620,6 +623,40 @@ def backward_timing(run, steps, warmup, bf16_peak, burst_peak, peak_src, sampler
             "roofline": roof, "gpu_launches_per_step": run.launches + 8, "clocks": clocks}
 
 
+def run_route_only(args):
+    """The routing stage alone (router GEMM + top-k + g, then the schedule) on
+    the workload's x and router weights, through moe_route_static: a small
+    device footprint (x and W_r only) for profiling the router kernel."""
+    import torch
+    import routing_grouped_expert_gemm_gb300 as rg
+    from routing_grouped_expert_gemm_gb300 import build as rgbuild
+    rgbuild.build()
+    shape = mi.CONFIGS[args.workload]
+    inp = mi.make_inputs(shape, weights=False)
+    T = min(shape.T, rg.MOE_ROUTE_STATIC_MAX_TOKENS)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    x, wr = dev(inp.x[:T]), dev(inp.w_router)
+    b = None if inp.b_router is None else torch.from_numpy(inp.b_router).cuda()
+    plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    o = [torch.empty((T, shape.k), **i32), torch.empty((T, shape.k), dtype=torch.float32, device="cuda"),
+         torch.empty(shape.E, **i32), torch.empty(shape.E + 1, **i32), torch.empty((T * shape.k, 3), **i32),
+         torch.empty(T * shape.k, **i32)]
+    for _ in range(args.warmup):
+        rg.moe_route_static(plan, T, x, wr, b, *o)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        rg.moe_route_static(plan, T, x, wr, b, *o)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / args.steps * 1000.0
+    print(json.dumps({"route_only": shape.name, "T": T, "us_per_call": us,
+                      "x_read_GB/s": T * shape.D * 2 / (us * 1e-6) / 1e9}), flush=True)
+    return 0
+
+
 def run_ours(args, world, rank, local):
     import torch
     import routing_grouped_expert_gemm_gb300 as rg
@@ -738,6 +775,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.route_only:
+        return run_route_only(args)
     return run_ours(args, world, rank, local)
 
 

@@ -116,7 +116,12 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
   const int w = (threadIdx.x >> 5) - 6;  // 0 or 1
   const bool lead = threadIdx.x == 6 * 32;
   for (int m = 0; m < p.n_mb; ++m) {
-    if (m >= p.slots) {  // ring slot m % slots free again: minibatch m - slots' up/gate tiles are done
+    const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
+    // a part with no M-tile in this minibatch only reports it done: it neither
+    // waits for the ring slot nor writes to it (with small minibatches most
+    // parts have none, and waiting would make every minibatch a grid-wide step)
+    const bool mine = part < ntile;
+    if (mine && m >= p.slots) {  // ring slot m % slots free again: minibatch m - slots' up/gate tiles are done
       if (lead)
         *s_gflag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), p.meta[META_MB + 4 * (m - p.slots)],
                                    p.status, p.timeout_ns) ? 1 : 0;
@@ -125,7 +130,6 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
     }
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
-    const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
     for (int i = part; i < ntile; i += parts) {
       const int mt = mt0 + i;
       const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
