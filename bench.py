@@ -623,6 +623,23 @@ def backward_timing(run, steps, warmup, bf16_peak, burst_peak, peak_src, sampler
             "roofline": roof, "gpu_launches_per_step": run.launches + 8, "clocks": clocks}
 
 
+def scheduling_comparison(run, steps, warmup):
+    """The one-CTA persistent kernel with its units claimed by the cooperative
+    grid from the global counter, against the same kernel scheduled by cluster
+    launch control (MoK Sec. 3.4: one CTA per task launched, running CTAs
+    cancel pending launches and take their tokens).  Same weights; the outputs
+    are bitwise equal (tests/test_gpu_clc.py)."""
+    out = {}
+    for name, clc in (("counter", 0), ("cluster_launch_control", 1)):
+        r = Runner(run.rg, run.torch, run.shape, run.inp, run.args, run.world, share=run, mma_pair=0, clc=clc)
+        res = r.timed(steps, warmup)
+        out[name] = {"ms_per_step": res["elapsed_ms"] / steps, "megakernel_ms": statistics.mean(res["mega_ms"]),
+                     "tokens_per_s": run.shape.T * steps / (res["elapsed_ms"] / 1000.0)}
+        del r
+    out["note"] = "one CTA per tile (mma_pair 0), the dispatch of the main line"
+    return out
+
+
 def run_route_only(args):
     """The routing stage alone (router GEMM + top-k + g, then the schedule) on
     the workload's x and router weights, through moe_route_static: a small
@@ -731,6 +748,7 @@ def run_ours(args, world, rank, local):
                                            ClockSampler(local))
     if not args.no_sweep and full_size:
         line["minibatch_sweep"] = minibatch_sweep(run, sweep_steps, 3)
+        line["scheduling"] = scheduling_comparison(run, sweep_steps, 3)
     cpu = None
     if world == 1 and not args.no_cpu_baseline and rank == 0:
         cb = time_oracle(inp, args.cpu_seconds)

@@ -106,6 +106,18 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              all 256 columns.  Ring or spread dispatch (direct gives
  *              MOE_ERR_INVALID_ARG); gather_ctas must be even.  Results are
  *              bitwise those of the one-CTA tiles.  0: one CTA per tile.
+ *   clc        1: the GEMM CTAs take their work tokens from cluster launch
+ *              control (MoK Sec. 3.4 "RDMA Overlap via Cluster Launch
+ *              Control"): the kernel is launched with one CTA per task beyond
+ *              the gather CTAs, not cooperatively; each running CTA cancels
+ *              the launch of a CTA that has not started and takes its token,
+ *              so when the hardware declines (a higher-priority stream wants
+ *              the SM) the CTA finishes its unit and leaves, and CTAs launched
+ *              later take the remaining units.  Which unit a token buys still
+ *              comes from the global counter in task order, so results are
+ *              bitwise those of the default scheduling.  One CTA per tile only
+ *              (mma_pair = 1 gives MOE_ERR_INVALID_ARG).  0: the persistent
+ *              cooperative grid claims units from the counter alone.
  *   test_unfilled_minibatch  test hook for the bounded waits, 0 in normal
  *              use: n >= 1 makes the ring fill never mark minibatch n - 1 as
  *              gathered, so the expert tiles waiting for it give up after
@@ -141,6 +153,7 @@ typedef struct moe_config {
   int32_t mma_pair;
   int32_t raster;
   int32_t test_unfilled_minibatch;
+  int32_t clc;
 } moe_config;
 
 /*

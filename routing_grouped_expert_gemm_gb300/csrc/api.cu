@@ -48,7 +48,7 @@ Layout make_layout(const moe_plan* pl, int64_t T) {
   const int64_t pad_seg = c.mma_pair ? L.max_segs : 0, pad_sh = c.mma_pair ? 1 : 0;
   L.n_tasks_max = (L.n_mtiles_max + pad_seg) * (c.I / BN_UP + c.D / BN_DOWN) +
                   (c.I_s > 0 ? (L.n_smtiles + pad_sh) * (c.I_s / BN_UP + c.D / BN_DOWN) : 0);
-  L.n_counters = 2 + 3 * L.n_mb + L.n_mtiles_max + L.n_smtiles;  // see ctr_claim
+  L.n_counters = 3 + 3 * L.n_mb + L.n_mtiles_max + L.n_smtiles;  // see ctr_claim, ctr_combine
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -188,6 +188,12 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.raster < 0) return MOE_ERR_INVALID_ARG;
   if (c.raster == 0) c.raster = 1 << 20;  // default: column-tile major over the whole segment
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
+  // cluster launch control schedules the one-CTA kernel
+  if (c.clc != 0 && c.clc != 1) return MOE_ERR_INVALID_ARG;
+  if (c.clc && c.mma_pair) return MOE_ERR_INVALID_ARG;
+#ifdef MOE_DEBUG_LOG
+  if (c.clc) return MOE_ERR_INVALID_ARG;  // the progress records are sized for the persistent grid
+#endif
   // the test hook needs a ring whose fill is signalled (ring or spread dispatch)
   if (c.test_unfilled_minibatch < 0 || (c.test_unfilled_minibatch > 0 && c.dispatch == MOE_DISPATCH_DIRECT))
     return MOE_ERR_INVALID_ARG;
@@ -358,6 +364,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.timeout_ns = (long long)c.timeout_ms * 1000000LL;
   p.l2_prefetch = c.l2_prefetch;
   p.test_unfilled = c.test_unfilled_minibatch;
+  p.clc = c.clc;
   p.x = static_cast<const bf16*>(x);
   p.b_router = w->b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);

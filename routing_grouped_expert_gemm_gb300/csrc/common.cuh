@@ -106,6 +106,7 @@ struct FwdParams {
   int n_counters;
   int l2_prefetch;      // K steps ahead that the producer prefetches into L2 (0 = off)
   int test_unfilled;    // test hook: 0 off; m + 1 = minibatch m is never marked gathered
+  int clc;              // 1: GEMM CTAs get their work tokens from cluster launch control (one-CTA kernel)
   long long timeout_ns;
   // inputs
   const bf16* x;
@@ -165,12 +166,15 @@ enum : int {
 #define TRACE_ADD(p, slot) (_trv[(slot)] += (unsigned long long)(clock64() - _tr0))
 #define TRACE_FLUSH(p)                                                                       \
   do {                                                                                       \
-    if ((p).trace)                                                                           \
+    if ((p).trace && blockIdx.x < 1024)                                                      \
       for (int _i = 2; _i < TRACE_SLOTS; ++_i)                                               \
         if (_trv[_i]) atomicAdd((p).trace + (size_t)blockIdx.x * TRACE_SLOTS + _i, _trv[_i]); \
   } while (0)
-#define TRACE_SET(p, slot, v) \
-  do { if ((p).trace) (p).trace[(size_t)blockIdx.x * TRACE_SLOTS + (slot)] = (unsigned long long)(v); } while (0)
+#define TRACE_SET(p, slot, v)                                                                  \
+  do {                                                                                         \
+    if ((p).trace && blockIdx.x < 1024)                                                        \
+      (p).trace[(size_t)blockIdx.x * TRACE_SLOTS + (slot)] = (unsigned long long)(v);          \
+  } while (0)
 #else
 #define TRACE_LOCALS() do {} while (0)
 #define TRACE_T0() do {} while (0)
@@ -231,7 +235,9 @@ __host__ __device__ inline size_t y_offset(const FwdParams& p, int t, int s, int
 }
 // the GEMM CTAs' unit claims (persistent kernel)
 __host__ __device__ inline int ctr_claim(const FwdParams& p) { return 1 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
-__host__ __device__ inline int n_counters(const FwdParams& p) { return 2 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
+// the combine's claims of round chunks (cluster-launch-control scheduling)
+__host__ __device__ inline int ctr_combine(const FwdParams& p) { return 2 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
+__host__ __device__ inline int n_counters(const FwdParams& p) { return 3 + 3 * p.n_mb + p.n_mtiles_max + p.n_smtiles; }
 
 struct TensorMaps {
   CUtensorMap x;        // [T, D]            box {64, 128}

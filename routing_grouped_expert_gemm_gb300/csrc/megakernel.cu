@@ -547,7 +547,12 @@ __device__ __forceinline__ void fma_f16x8(float* acc, float g, uint4 w) {
 }
 
 // buf: buf_bytes of shared memory free for the pass; bars: CMB_BUFS free
-// mbarrier slots; ok: a shared flag.  Every thread of the CTA calls it.
+// mbarrier slots; ok: a shared flag.  Every thread of the CTA calls it.  The
+// rounds are split statically over the grid's CTAs, or (cluster launch
+// control: the grid is far larger than the CTAs that run) claimed in chunks of
+// CMB_CHUNK rounds from a global counter.  Which CTA sums a unit does not
+// change its arithmetic.
+constexpr int CMB_CHUNK = 16;
 __device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, uint64_t* bars, volatile int* ok) {
   const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
   const int warps = (int)(blockDim.x >> 5);  // units per round
@@ -559,69 +564,94 @@ __device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, ui
   const long long per_tt = (long long)p.N2 * BM;              // units of one token tile
   const long long n_units = (long long)((p.T + BM - 1) / BM) * per_tt;
   const long long n_rounds = (n_units + warps - 1) / warps;
-  const long long per_cta = (n_rounds + gridDim.x - 1) / gridDim.x;
-  const long long r0 = (long long)blockIdx.x * per_cta;
-  const int nr = (int)max(0ll, min(n_rounds, r0 + per_cta) - r0);
   if (threadIdx.x == 0) {
     for (int i = 0; i < nb; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
-  auto issue = [&](int i) {  // this CTA's round i into buffer i % nb
-    const long long u = (r0 + i) * warps;
-    const uint32_t bytes = (uint32_t)min((long long)warps, n_units - u) * unit_bytes;
-    mbar_arrive_expect_tx(&bars[i % nb], bytes);
-    bulk_load(buf + (size_t)(i % nb) * round_bytes, p.Y + (size_t)u * kY * BN_DOWN, bytes, &bars[i % nb]);
-  };
-  if (threadIdx.x == 0)
-    for (int i = 0; i < min(nb, nr); ++i) issue(i);
-  int issued = min(nb, nr);  // thread 0: rounds whose copies were issued
-  // router weights of the warp's next unit, loaded a round ahead: lane s holds slot s
-  auto unit_tok = [&](int i) {
-    const long long u = (r0 + i) * warps + warp;
-    const int t = (int)(u / per_tt) * BM + (int)(u % BM);
-    return (i < nr && u < n_units && t < p.T) ? t : -1;
-  };
-  int tok = unit_tok(0);
-  float g = tok >= 0 && lane < k ? p.topk_w[(size_t)tok * k + lane] : 0.0f;
-  int i = 0;
-  for (; i < nr; ++i) {
-    if (threadIdx.x == 0) *ok = mbar_wait(&bars[i % nb], (uint32_t)(i / nb) & 1u, p.status, p.timeout_ns) ? 1 : 0;
-    __syncthreads();  // also: every warp is done with round i - 1
-    if (*ok == 0) break;
-    if (threadIdx.x == 0 && i >= 1 && i - 1 + nb < nr) {  // refill the buffer round i - 1 used
-      fence_proxy_async_smem();
-      issue(i - 1 + nb);
-      ++issued;
+  volatile long long* s_r0 = reinterpret_cast<volatile long long*>(bars + CMB_BUFS);
+  uint32_t seq = 0;  // rounds this CTA has streamed so far (buffer = seq % nb, phase = (seq / nb) & 1)
+  for (int range = 0;; ++range) {
+    long long r0;
+    int nr;
+    if (p.clc) {
+      if (threadIdx.x == 0) *s_r0 = (long long)atomicAdd(p.counters + ctr_combine(p), 1) * CMB_CHUNK;
+      __syncthreads();
+      r0 = *s_r0;
+      nr = (int)max(0ll, min(n_rounds, r0 + CMB_CHUNK) - r0);
+    } else {
+      if (range > 0) break;
+      const long long per_cta = (n_rounds + gridDim.x - 1) / gridDim.x;
+      r0 = (long long)blockIdx.x * per_cta;
+      nr = (int)max(0ll, min(n_rounds, r0 + per_cta) - r0);
     }
-    const int tok_next = unit_tok(i + 1);
-    const float g_next = tok_next >= 0 && lane < k ? p.topk_w[(size_t)tok_next * k + lane] : 0.0f;
-    if (tok >= 0) {
-      const __half* y = reinterpret_cast<const __half*>(buf + (size_t)(i % nb) * round_bytes +
-                                                        (size_t)warp * unit_bytes) + 8 * lane;
-      float acc[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-      if (shared) fma_f16x8(acc, 1.0f, *reinterpret_cast<const uint4*>(y + (size_t)k * BN_DOWN));  // exact
-#pragma unroll 4
-      for (int s = 0; s < k; ++s)
-        fma_f16x8(acc, __shfl_sync(0xffffffffu, g, s), *reinterpret_cast<const uint4*>(y + (size_t)s * BN_DOWN));
+    if (nr == 0) break;
+    auto issue = [&](int i) {  // this range's round i into buffer (seq + i) % nb
+      const uint32_t q = seq + (uint32_t)i;
+      const long long u = (r0 + i) * warps;
+      const uint32_t bytes = (uint32_t)min((long long)warps, n_units - u) * unit_bytes;
+      mbar_arrive_expect_tx(&bars[q % nb], bytes);
+      bulk_load(buf + (size_t)(q % nb) * round_bytes, p.Y + (size_t)u * kY * BN_DOWN, bytes, &bars[q % nb]);
+    };
+    __syncthreads();  // every warp is done with the previous range's buffers
+    if (threadIdx.x == 0) {
+      fence_proxy_async_smem();
+      for (int i = 0; i < min(nb, nr); ++i) issue(i);
+    }
+    int issued = min(nb, nr);  // thread 0: rounds whose copies were issued
+    // router weights of the warp's next unit, loaded a round ahead: lane s holds slot s
+    auto unit_tok = [&](int i) {
       const long long u = (r0 + i) * warps + warp;
-      const int n = (int)((u / BM) % p.N2);
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(p.out + (size_t)tok * p.D + n * BN_DOWN + 8 * lane) = o;
-    }  // (tok is the same for the whole warp: all lanes or none take part in the shuffles)
-    tok = tok_next;
-    g = g_next;
+      const int t = (int)(u / per_tt) * BM + (int)(u % BM);
+      return (i < nr && u < n_units && t < p.T) ? t : -1;
+    };
+    int tok = unit_tok(0);
+    float g = tok >= 0 && lane < k ? p.topk_w[(size_t)tok * k + lane] : 0.0f;
+    int i = 0;
+    for (; i < nr; ++i) {
+      const uint32_t q = seq + (uint32_t)i;
+      if (threadIdx.x == 0) *ok = mbar_wait(&bars[q % nb], (q / nb) & 1u, p.status, p.timeout_ns) ? 1 : 0;
+      __syncthreads();  // also: every warp is done with round i - 1
+      if (*ok == 0) break;
+      if (threadIdx.x == 0 && i >= 1 && i - 1 + nb < nr) {  // refill the buffer round i - 1 used
+        fence_proxy_async_smem();
+        issue(i - 1 + nb);
+        ++issued;
+      }
+      const int tok_next = unit_tok(i + 1);
+      const float g_next = tok_next >= 0 && lane < k ? p.topk_w[(size_t)tok_next * k + lane] : 0.0f;
+      if (tok >= 0) {
+        const __half* y = reinterpret_cast<const __half*>(buf + (size_t)(q % nb) * round_bytes +
+                                                          (size_t)warp * unit_bytes) + 8 * lane;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        if (shared) fma_f16x8(acc, 1.0f, *reinterpret_cast<const uint4*>(y + (size_t)k * BN_DOWN));  // exact
+#pragma unroll 4
+        for (int s = 0; s < k; ++s)
+          fma_f16x8(acc, __shfl_sync(0xffffffffu, g, s), *reinterpret_cast<const uint4*>(y + (size_t)s * BN_DOWN));
+        const long long u = (r0 + i) * warps + warp;
+        const int n = (int)((u / BM) % p.N2);
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(p.out + (size_t)tok * p.D + n * BN_DOWN + 8 * lane) = o;
+      }  // (tok is the same for the whole warp: all lanes or none take part in the shuffles)
+      tok = tok_next;
+      g = g_next;
+    }
+    // copies still in flight (an abort) land before the CTA leaves
+    if (threadIdx.x == 0)
+      for (int j = i; j < issued; ++j) {
+        const uint32_t q = seq + (uint32_t)j;
+        mbar_wait_drain(&bars[q % nb], (q / nb) & 1u, p.timeout_ns);
+      }
+    __syncthreads();
+    seq += (uint32_t)issued;
+    if (*ok == 0) break;
   }
-  // copies still in flight (an abort) land before the CTA leaves
-  if (threadIdx.x == 0)
-    for (int j = i; j < issued; ++j) mbar_wait_drain(&bars[j % nb], (uint32_t)(j / nb) & 1u, p.timeout_ns);
-  __syncthreads();
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -697,7 +727,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   uint8_t* smem = align_1024_mk(smem_raw);
   uint8_t* sf_slots = smem + NST * G::stride;  // pairs with MXFP8 tiles: scale blocks per stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf_slots + G::sf_bytes);
-  static_assert(2 * 6 + 7 <= 24 && 48 * 8 + QN * 4 <= BAR_BYTES, "barrier area");
+  static_assert(2 * 6 + 7 <= 24 && 48 * 8 + QN * 4 <= 52 * 8 && 56 * 8 <= BAR_BYTES, "barrier area");
   uint64_t* full = bars;
   uint64_t* empty = bars + NST;
   uint64_t* tfull = bars + 2 * NST;
@@ -710,6 +740,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   uint64_t* qfull = bars + 32;       // unit queue: slot written
   uint64_t* qempty = bars + 40;      // ... slot read by every reader
   volatile int* qslot = reinterpret_cast<volatile int*>(bars + 48);
+  uint64_t* clc_bar = bars + 52;     // cluster launch control: the response's barrier ...
+  void* clc_resp = bars + 54;        // ... and the 16-byte response (16-byte aligned)
   EpiStage* epi = reinterpret_cast<EpiStage*>(sf_slots + G::sf_bytes + BAR_BYTES);
 #ifdef MOE_TRACE
   volatile uint64_t* s_issue_ns = bars + 24;  // per stage: when its loads were issued (trace builds)
@@ -717,6 +749,12 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_gather = (int)blockIdx.x < p.G;
+  // cluster launch control: the grid has one CTA per task of the largest
+  // possible task list; a CTA launched past the actual list only starts once
+  // every real task's token is spent (launches go in index order, and the
+  // running CTAs cancel in that order), so it has nothing to do
+  // (the first n_gemm GEMM CTAs also fill the ring in spread dispatch: they stay)
+  if (!kPair && p.clc && !is_gather && (int)blockIdx.x - p.G >= max(p.meta[META_N_TASKS], p.n_gemm)) return;
   if (threadIdx.x == 0) {
     atomicMin(p.stamps + STAMP_START, (unsigned long long)globaltimer_ns());
     TRACE_SET(p, TR_START_NS, globaltimer_ns());
@@ -748,6 +786,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         mbar_init(&thead[a], kPair ? 8 : 128);
       }
       mbar_init(drain, 1);
+      mbar_init(clc_bar, 1);
       for (int i = 0; i < QN; ++i) {
         mbar_init(&qfull[i], 1);
         mbar_init(&qempty[i], kPair ? 4 : 2);  // MMA issuer + epilogue (pairs: + the odd CTA's producer and epilogue)
@@ -794,7 +833,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
-      int claim = 0;  // even / only CTA: the unit claimed for the next queue slot
+      // even / only CTA: the unit claimed for the next queue slot.  Every
+      // claim takes the next unit from the global counter, so the claimed
+      // units are always a prefix of the task order.  With cluster launch
+      // control a claim also needs a work token: this CTA's own launch, then
+      // one launch of this grid cancelled before it started (requested while
+      // the previous unit loads); no token, no further claim.
+      int claim = 0;
+      bool clc_pending = false;
+      uint32_t clc_phase = 0;
       if (lead_lane && leader) claim = atomicAdd(p.counters + ctr_claim(p), 1);
       for (int i = 0; ok; ++i) {
         const int slot = i % QN;
@@ -802,6 +849,17 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         int u = -2;  // -2: a wait ran out; -1: no units left
         if (lead_lane) {
           if (leader) {  // publish the claimed unit, then claim the one after it
+            if (clc_pending) {
+              clc_pending = false;
+              uint32_t cx = 0;
+              if (!mbar_wait(clc_bar, clc_phase, p.status, p.timeout_ns)) {
+                claim = INT_MAX;
+              } else {
+                clc_phase ^= 1u;
+                claim = (clc_query(clc_resp, &cx) && (int)cx >= p.G) ? atomicAdd(p.counters + ctr_claim(p), 1)
+                                                                    : INT_MAX;
+              }
+            }
             if (wait_bar(&qempty[slot], qpar ^ 1u)) {
               u = claim < walk.n_units ? claim : -1;
               qslot[slot] = u;
@@ -810,7 +868,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
                 mbar_arrive_remote_cluster(qfull_odd + 8u * slot);
               }
               mbar_arrive(&qfull[slot]);
-              if (u >= 0) claim = atomicAdd(p.counters + ctr_claim(p), 1);
+              if (u >= 0) {
+                if (!kPair && p.clc) {
+                  mbar_arrive_expect_tx(clc_bar, 16u);
+                  clc_try_cancel(clc_resp, clc_bar);
+                  clc_pending = true;
+                } else {
+                  claim = atomicAdd(p.counters + ctr_claim(p), 1);
+                }
+              }
             }
           } else if (wait_bar(&qfull[slot], qpar)) {  // odd CTA: the even CTA's unit
             u = qslot[slot];
@@ -971,6 +1037,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
       }
+      // a cancellation request still in flight is answered before the CTA leaves
+      if (lead_lane && clc_pending) mbar_wait_drain(clc_bar, clc_phase, p.timeout_ns);
       // the last loads issued have landed before the CTA may leave (pairs: the
       // even CTA's full barriers count both CTAs' loads, and the odd CTA waits
       // for the even one at the cluster barrier below)
@@ -1107,7 +1175,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
       __syncwarp();
     } else if (warp >= 6) {
       // ---------------- ring fill spread over the GEMM CTAs
-      if (p.spread) gather_role_spread(p, cta, p.n_gemm, s_ok + 1);
+      if (p.spread && cta < p.n_gemm) gather_role_spread(p, cta, p.n_gemm, s_ok + 1);
     } else if (warp >= 2 && warp < 6) {
       // ---------------- epilogue
       const int q = warp & 3;
@@ -1216,11 +1284,16 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
     }
   }
 
-  // ---------------- combine: every CTA, once every staging row is stored
+  // ---------------- combine: every CTA, once every staging row is stored.
+  // Cluster launch control: a GEMM CTA whose cancellation request was declined
+  // while units were still unclaimed yields its SM at once (CTAs of this grid
+  // launched later take the rest, and the combine is claimed in chunks).
   if (threadIdx.x == 0) {
     TRACE_LOCALS();
     TRACE_T0();
-    *s_flag = wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns) ? 1 : 0;
+    const bool yield = p.clc && !is_gather && ld_relaxed_gpu(p.counters + ctr_claim(p)) < p.meta[META_N_TASKS];
+    *s_flag = !yield && wait_counter_ge(p.counters + ctr_ydone(), p.meta[META_TOTAL_Y], p.status, p.timeout_ns)
+                  ? 1 : 0;
     if (*s_flag) atomicMin(p.stamps + STAMP_COMBINE_START, (unsigned long long)globaltimer_ns());
     TRACE_ADD(p, TR_FINAL_WAIT);
     TRACE_FLUSH(p);
@@ -1234,7 +1307,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
                  reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi) + CMB_BAR_OFFSET), s_ok);
     if (threadIdx.x == 0) atomicMax(p.stamps + STAMP_COMBINE_END, (unsigned long long)globaltimer_ns());
 #ifdef MOE_TRACE
-    if (threadIdx.x == 0 && p.trace) p.trace[(size_t)blockIdx.x * TRACE_SLOTS + TR_COMBINE] = clock64() - c0;
+    if (threadIdx.x == 0 && p.trace && blockIdx.x < 1024) p.trace[(size_t)blockIdx.x * TRACE_SLOTS + TR_COMBINE] = clock64() - c0;
 #endif
   }
   __syncthreads();
@@ -1264,6 +1337,9 @@ __global__ void __launch_bounds__(MEGA_THREADS, 1)
 
 cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int grid, cudaStream_t stream) {
   const bool pair = p.pair != 0, pair_mx = pair && p.mx;
+  // cluster launch control: one CTA per task beyond the gather CTAs; the CTAs
+  // that run cancel the launches of the others and take their tokens
+  if (p.clc && !pair) grid = p.G + p.n_tasks_max;
   const void* fn = pair_mx ? reinterpret_cast<const void*>(moe_megakernel_pair_mx)
                    : pair  ? reinterpret_cast<const void*>(moe_megakernel_pair)
                            : reinterpret_cast<const void*>(moe_megakernel);
@@ -1285,7 +1361,7 @@ cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int gr
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pair ? 2 : 1;
+  cfg.numAttrs = pair ? 2 : (p.clc ? 0 : 1);  // cluster launch control: not cooperative (the grid exceeds the SMs)
   if (pair_mx) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair_mx, maps, p);
   if (pair) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair, maps, p);
   return cudaLaunchKernelEx(&cfg, moe_megakernel, maps, p);

@@ -266,6 +266,31 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
+// ------------------------------------------------------------------ cluster launch control
+// Ask the hardware to cancel the launch of a not-yet-started cluster of this
+// grid; the 16-byte response lands at `resp` (16-byte aligned shared memory)
+// and completes 16 bytes of transaction on `bar` (the caller sets expect_tx).
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                   smem_u32(resp)),
+               "r"(smem_u32(bar))
+               : "memory");
+}
+// Decode a response: true and the canceled cluster's first CTA index (x) if a
+// launch was canceled, false if none was (none left, or the hardware declined).
+__device__ __forceinline__ bool clc_query(const void* resp, uint32_t* ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b128 q;\n ld.shared.b128 q, [%2];\n"
+      " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, q;\n selp.u32 %0, 1, 0, p;\n"
+      " clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, q;\n}\n"
+      : "=r"(ok), "=r"(x)
+      : "r"(smem_u32(resp))
+      : "memory");
+  *ctaid_x = x;
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ tcgen05
 template <uint32_t kCols>
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem) {  // whole warp

@@ -71,7 +71,7 @@ constexpr RouteLayout route_layout(int64_t T, int64_t E, int64_t k) {
   L.n_chunks = (int)((T + BM - 1) / BM);
   L.max_segs = L.n_mb + (int)E;
   L.n_mtiles_max = (int)((R + BM - 1) / BM) + L.n_mb + (int)E;
-  L.n_counters = 2 + 3 * L.n_mb + L.n_mtiles_max;
+  L.n_counters = 3 + 3 * L.n_mb + L.n_mtiles_max;
   size_t off = 0;
   L.status = off;  // status word, warning bits, phase stamps
   off = align256(off + STATUS_AREA_BYTES);

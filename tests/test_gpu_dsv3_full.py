@@ -7,7 +7,8 @@ configuration: the benchmark's (CTA pairs; ring dispatch with 8 gather CTAs
 for BF16, spread for MXFP8), the minibatch sizes 512, 2048 and 32768 that
 "Mixture-of-Kittens: MoE Megakernel for NVL72s" sweeps (Sec. 3.2, Fig. 5;
 32768 x 4 ring slots holds all T*k routes: the over-allocated buffer of
-Sec. 3.3), and the one-CTA kernel with each dispatch mode.
+Sec. 3.3), the one-CTA kernel with each dispatch mode, and the one-CTA kernel
+scheduled by cluster launch control.
 
 Bars: routing (top-k, g, counts, offsets, schedule, its inverse) on every
 token; outputs on a 1024-token sample that holds every token routed to the
@@ -37,6 +38,7 @@ BF16_CONFIGS = [  # (name, plan knobs); the first is the benchmark's
     ("one_cta_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=8)),
     ("one_cta_direct", dict(minibatch=8192, ring_slots=4, dispatch="direct")),
     ("one_cta_spread", dict(minibatch=8192, ring_slots=4, dispatch="spread")),
+    ("one_cta_ring_clc", dict(minibatch=8192, ring_slots=4, gather_ctas=8, clc=1)),
 ]
 MX_CONFIGS = [
     ("bench", dict(minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)),
@@ -46,6 +48,7 @@ MX_CONFIGS = [
     ("pair_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=6, mma_pair=1)),
     ("one_cta_direct", dict(minibatch=8192, ring_slots=4, dispatch="direct")),
     ("one_cta_spread", dict(minibatch=8192, ring_slots=4, dispatch="spread")),
+    ("one_cta_spread_clc", dict(minibatch=8192, ring_slots=4, dispatch="spread", clc=1)),
 ]
 
 
