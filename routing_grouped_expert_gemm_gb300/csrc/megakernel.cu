@@ -108,8 +108,8 @@ __device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, 
 }
 
 // Ring fill spread over the GEMM CTAs (MOE_DISPATCH_SPREAD): warps 6 and 7
-// of GEMM CTA `part` (of `parts`) copy the rows of the minibatch's M-tiles
-// part, part + parts, ... through registers, while the CTA's other warps run
+// of GEMM CTA `part` (of `parts`) copy the rows of the M-tiles mt with
+// mt % parts == part through registers, while the CTA's other warps run
 // expert tiles; every part adds 1 to the minibatch's fill counter.  They sync
 // among themselves with named barrier 2 (64 threads).
 __device__ void gather_role_spread(const FwdParams& p, int part, int parts, volatile int* s_gflag) {
@@ -117,10 +117,13 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
   const bool lead = threadIdx.x == 6 * 32;
   for (int m = 0; m < p.n_mb; ++m) {
     const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
-    // a part with no M-tile in this minibatch only reports it done: it neither
-    // waits for the ring slot nor writes to it (with small minibatches most
-    // parts have none, and waiting would make every minibatch a grid-wide step)
-    const bool mine = part < ntile;
+    // M-tile mt of the run goes to part mt % parts, so that with small
+    // minibatches (few M-tiles each) the fill still rotates over every part.
+    // A part with no M-tile in this minibatch only reports it done: it neither
+    // waits for the ring slot nor writes to it (waiting would make every
+    // minibatch a grid-wide step)
+    const int i0 = ((part - mt0) % parts + parts) % parts;  // this part's first tile of the minibatch
+    const bool mine = i0 < ntile;
     if (mine && m >= p.slots) {  // ring slot m % slots free again: minibatch m - slots' up/gate tiles are done
       if (lead)
         *s_gflag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), p.meta[META_MB + 4 * (m - p.slots)],
@@ -130,7 +133,7 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
     }
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
-    for (int i = part; i < ntile; i += parts) {
+    for (int i = i0; i < ntile; i += parts) {
       const int mt = mt0 + i;
       const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
       for (int r = w; r < rows; r += 2) {
@@ -649,8 +652,8 @@ __device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, ui
         mbar_wait_drain(&bars[q % nb], (q / nb) & 1u, p.timeout_ns);
       }
     __syncthreads();
-    seq += (uint32_t)issued;
     if (*ok == 0) break;
+    seq += (uint32_t)nr;  // every round of the range was streamed (only thread 0 counts `issued`)
   }
 }
 

@@ -50,6 +50,20 @@ def test_clc_matches_default_scheduling_bitwise(dispatch, precision):
         assert torch.equal(got[key], ref[key]), key
 
 
+def test_clc_combine_over_several_chunks_per_cta():
+    """Enough combine rounds (4096 tokens x 8 column tiles) that CTAs claim
+    several chunks each: the chunked combine must still be bitwise the default."""
+    import gpu_util
+    inp = _small(4096, 2048, 256, 16, 4, 256, cid=802)
+    x = gpu_util.to_dev_bf16(inp.x)
+    ref_layer = gpu_util.Layer(inp, minibatch=4096, ring_slots=2, gather_ctas=4)
+    ref = ref_layer.run(x)
+    layer = gpu_util.Layer(inp, weights=ref_layer.w, minibatch=4096, ring_slots=2, gather_ctas=4, clc=1)
+    got = layer.run(x, poison=True)
+    assert ref["status"] == 0 and got["status"] == 0
+    assert torch.equal(got["out"].view(torch.int16), ref["out"].view(torch.int16))
+
+
 def test_clc_tiny_all_tokens_against_oracle():
     import gpu_util
     inp = mi.make_inputs("tiny")
