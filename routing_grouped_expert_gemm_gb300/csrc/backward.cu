@@ -52,9 +52,7 @@ constexpr int BWD_QN = 8;
 constexpr int BOXB = 8192;         // one {64, 64} bf16 box: 64 rows x 128 B
 constexpr int PADK = 64;           // an expert's routes padded to a multiple of 64 (one K step)
 constexpr int WR_CHUNK = 256;      // routes per router-gradient partial sum
-constexpr int BWD_BAR_BYTES = 512;
-constexpr int BWD_EPI_BYTES = 4 * 4224;  // one 32 x 33-float staging block per epilogue warp
-constexpr int BWD_SMEM = BWD_STAGES * BWD_STAGE + 1024 + BWD_BAR_BYTES + BWD_EPI_BYTES;
+constexpr int BWD_SMEM = BWD_STAGES * BWD_STAGE + 1024 + 512;
 
 enum : int {
   BU_A_ROUTED = 0, BU_A_SHARED, BU_DX_ROUTED, BU_DX_SHARED, BU_DW_DOWN, BU_DW_UP, BU_DW_GATE, BU_DWS_DOWN,
@@ -415,68 +413,35 @@ __device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams
 }
 
 // ------------------------------------------------------------------ epilogue helpers
-// A warp's 32 rows (one per lane, TMEM lanes) x 32 columns are restaged
-// through shared memory (row stride 33 floats: conflict-free both ways) so
-// that lane l then handles row 4i + l/8, columns 4 (l % 8) .. +3: every warp
-// store covers 4 rows x 64 contiguous bytes instead of 32 rows x 16 bytes.
-struct BStage {
-  float v[32][33];
-};
-static_assert(sizeof(BStage) * 4 == BWD_EPI_BYTES, "epilogue staging size");
-
-__device__ __forceinline__ void bstage(BStage& st, const float* v) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) st.v[lane][j] = v[j];
-  __syncwarp();
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
 }
-// row `lane` of the block goes to base + my_off (elements), skipped where my_off < 0
-__device__ __forceinline__ void bstore_bf16(BStage& st, const float* v, bf16* base, long long my_off) {
-  bstage(st, v);
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
-    const long long off = __shfl_sync(0xffffffffu, my_off, rr);
-    if (off >= 0) {
-      const float* f = &st.v[rr][cc];
-      *reinterpret_cast<uint2*>(base + off + cc) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-    }
-  }
-  __syncwarp();
-}
-// the same into fp16, saturated at +-65504; true if a stored value left that range (or is NaN)
-__device__ __forceinline__ bool bstore_f16_sat(BStage& st, const float* v, __half* base, long long my_off) {
-  bstage(st, v);
-  const int lane = threadIdx.x & 31;
+// fp16 with saturation at +-65504; returns true if a value left that range (or is NaN)
+__device__ __forceinline__ bool store_f16x32_sat(__half* dst, const float* v) {
   bool bad = false;
+  uint32_t w[16];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
-    const long long off = __shfl_sync(0xffffffffu, my_off, rr);
-    if (off >= 0) {
-      const float* f = &st.v[rr][cc];
-      uint32_t w[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float a = f[2 * q], b = f[2 * q + 1];
-        bad |= !(fabsf(a) <= 65504.0f) || !(fabsf(b) <= 65504.0f);
-        __half2 h = __floats2half2_rn(fminf(fmaxf(a, -65504.0f), 65504.0f), fminf(fmaxf(b, -65504.0f), 65504.0f));
-        w[q] = *reinterpret_cast<uint32_t*>(&h);
-      }
-      *reinterpret_cast<uint2*>(base + off + cc) = make_uint2(w[0], w[1]);
-    }
+  for (int i = 0; i < 16; ++i) {
+    const float a = v[2 * i], b = v[2 * i + 1];
+    bad |= !(fabsf(a) <= 65504.0f) || !(fabsf(b) <= 65504.0f);
+    __half2 h = __floats2half2_rn(fminf(fmaxf(a, -65504.0f), 65504.0f), fminf(fmaxf(b, -65504.0f), 65504.0f));
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
   }
-  __syncwarp();
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   return bad;
 }
 
 // Phase 0 epilogue of one row (TMEM lane): columns [0,128) up, [128,256) gate,
-// [256,384) dh'.  Writes g h, da_u, da_g (bf16) for 128 columns of I at
-// element offset my_off of each output (< 0: not stored) and returns this
-// row's part of dg = <dh', h> (fp32, columns in order).
-__device__ __forceinline__ float epi_act_grad(uint32_t taddr, float g, BStage& st, long long my_off, bf16* hg,
-                                              bf16* dau, bf16* dag) {
+// [256,384) dh'.  Writes g h, da_u, da_g (bf16) for 128 columns of I and
+// returns this row's part of dg = <dh', h> (fp32, columns in order).
+__device__ __forceinline__ float epi_act_grad(uint32_t taddr, float g, bool store, bf16* hg_row, bf16* dau_row,
+                                              bf16* dag_row) {
   float dg = 0.0f;
 #pragma unroll 1
   for (int c = 0; c < BN_UP; c += 32) {
@@ -498,9 +463,11 @@ __device__ __forceinline__ float epi_act_grad(uint32_t taddr, float g, BStage& s
       vu[j] = dh * si;
       vg[j] = dh * au * sg * (1.0f + ag * (1.0f - sg));
     }
-    bstore_bf16(st, vh, hg + c, my_off);
-    bstore_bf16(st, vu, dau + c, my_off);
-    bstore_bf16(st, vg, dag + c, my_off);
+    if (store) {
+      store_bf16x32(hg_row + c, vh);
+      store_bf16x32(dau_row + c, vu);
+      store_bf16x32(dag_row + c, vg);
+    }
   }
   return dg;
 }
@@ -527,8 +494,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
   volatile int* s_unit = qslot + BWD_QN;
   volatile int* s_ok = s_unit + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(s_ok + 1));
-  BStage* epi = reinterpret_cast<BStage*>(smem + BWD_STAGES * BWD_STAGE + BWD_BAR_BYTES);
-  static_assert((2 * BWD_STAGES + 4 + 2 * BWD_QN + 1) * 8 + (BWD_QN + 3) * 4 <= BWD_BAR_BYTES, "barrier area");
+  static_assert((2 * BWD_STAGES + 4 + 2 * BWD_QN + 1) * 8 + (BWD_QN + 3) * 4 <= 512, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_units = bwd_units(p, PHASE);
@@ -680,19 +646,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
       if (*s_ok == 0) break;
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * 256u;
-      BStage& st = epi[q];
       if (b.kind == BU_A_ROUTED) {
         const bool valid = rloc < b.rows;
         const int prow = b.a_row + rloc;
         const int j = valid ? p.prow_route[prow] : -1;
         const float g = j >= 0 ? p.topk_w[j] : 0.0f;  // padding rows: all zero
-        const long long o = valid ? (long long)prow * p.I + b.n * BN_UP : -1;
-        const float dg = epi_act_grad(taddr, g, st, o, p.hg, p.dau, p.dag);
+        const size_t o = (size_t)prow * p.I + b.n * BN_UP;
+        const float dg = epi_act_grad(taddr, g, valid, p.hg + o, p.dau + o, p.dag + o);
         if (j >= 0) p.dgp[(size_t)prow * p.N1 + b.n] = dg;
       } else if (b.kind == BU_A_SHARED) {
         const int t = b.a_row + rloc;
-        const long long o = t < p.T ? (long long)t * p.I_s + b.n * BN_UP : -1;
-        epi_act_grad(taddr, 1.0f, st, o, p.hs, p.dasu, p.dasg);
+        const bool valid = t < p.T;
+        const size_t o = (size_t)(valid ? t : 0) * p.I_s + b.n * BN_UP;
+        epi_act_grad(taddr, 1.0f, valid, p.hs + o, p.dasu + o, p.dasg + o);
       } else if (b.kind == BU_DX_ROUTED || b.kind == BU_DX_SHARED) {
         int srow = -1;  // staging row t kY + slot
         if (b.kind == BU_DX_ROUTED) {
@@ -710,7 +676,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
           float v[32];
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) v[jj] = __uint_as_float(r[jj]);
-          ovf |= bstore_f16_sat(st, v, p.dxs + c, srow >= 0 ? (long long)srow * p.D + b.n * 256 : -1);
+          if (srow >= 0) ovf |= store_f16x32_sat(p.dxs + (size_t)srow * p.D + b.n * 256 + c, v);
         }
       } else {  // weight gradient tile: rows m*128 + rloc, columns n*256 ...
         bf16* out;
@@ -723,7 +689,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
           case BU_DWS_UP: out = p.dWs_up; ld = p.D; break;
           default: out = p.dWs_gate; ld = p.D; break;
         }
-        const long long my_off = (long long)(b.m * BM + rloc) * ld + b.n * 256;
+        bf16* row = out + (size_t)(b.m * BM + rloc) * ld + b.n * 256;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           float v[32];
@@ -737,7 +703,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) v[jj] = 0.0f;
           }
-          bstore_bf16(st, v, out + c, my_off);
+          store_bf16x32(row + c, v);
         }
       }
       tc_fence_before();
