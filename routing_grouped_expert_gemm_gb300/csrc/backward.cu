@@ -52,7 +52,12 @@ constexpr int BWD_QN = 8;
 constexpr int BOXB = 8192;         // one {64, 64} bf16 box: 64 rows x 128 B
 constexpr int PADK = 64;           // an expert's routes padded to a multiple of 64 (one K step)
 constexpr int WR_CHUNK = 256;      // routes per router-gradient partial sum
-constexpr int BWD_SMEM = BWD_STAGES * BWD_STAGE + 1024 + 512;
+constexpr int BWD_BAR_BYTES = 512;
+constexpr int BWD_SMEM = BWD_STAGES * BWD_STAGE + 1024 + BWD_BAR_BYTES;
+// CTA pairs: per CTA and stage its A (16 KB) and its half of B (up to 16 KB)
+constexpr int BWD_PAIR_STAGES = 6;
+constexpr int BWD_PAIR_STAGE = 32768;
+constexpr int BWD_PAIR_SMEM = BWD_PAIR_STAGES * BWD_PAIR_STAGE + 1024 + BWD_BAR_BYTES;
 
 enum : int {
   BU_A_ROUTED = 0, BU_A_SHARED, BU_DX_ROUTED, BU_DX_SHARED, BU_DW_DOWN, BU_DW_UP, BU_DW_GATE, BU_DWS_DOWN,
@@ -73,6 +78,7 @@ struct BwdParams {
   int N1, N1s, N2;        // I/128, I_s/128, D/256 column tiles
   int n_tt;               // token tiles ceil(T/128)
   int n_mt_max, Rp_max, n_wc_max;
+  int pair;               // 1: CTA pairs (cta_group::2); M-tile entries are pairs of tiles
   long long timeout_ns;
   // the forward's routing and schedule (its workspace)
   const int* topk_idx;
@@ -92,7 +98,8 @@ struct BwdParams {
   int* Sp;                // [E + 1] padded segment starts
   int* wc0;               // [E + 1] first router-gradient chunk of each expert
   int* eorder;            // [E] experts by descending route count
-  int* mtiles;            // [n_mt_max, 4] {e, first padded row, rows, -}
+  int* mtiles;            // [n_mt_max, 4] {e, first padded row, rows, -}; pairs: {e, first row, rows of
+                          // the first tile, rows of the second (0: an empty partner)}
   int* prow_route;        // [Rp_max] route of a padded row, -1 for padding
   int* route_prow;        // [T k] padded row of a route
   bf16* xg;               // [Rp_max, D]
@@ -152,13 +159,14 @@ __global__ void __launch_bounds__(512, 1) bwd_prep(BwdParams p) {
   __syncthreads();
   if (tid == 0) {  // E <= 512: serial scans in fixed order
     int sp = 0, mt = 0, wc = 0;
+    const int tile_rows = p.pair ? 2 * BM : BM;  // rows of one M-tile entry
     for (int e = 0; e < E; ++e) {
       const int m64 = (sM[e] + PADK - 1) / PADK * PADK;
       sPad[e] = sp;
       sTiles[e] = mt;
       sChunk[e] = wc;
       sp += m64;
-      mt += (m64 + BM - 1) / BM;
+      mt += (m64 + tile_rows - 1) / tile_rows;
       wc += (sM[e] + WR_CHUNK - 1) / WR_CHUNK;
     }
     sPad[E] = sp;
@@ -179,12 +187,13 @@ __global__ void __launch_bounds__(512, 1) bwd_prep(BwdParams p) {
     for (int f = 0; f < E; ++f) rank += (sM[f] > sM[e] || (sM[f] == sM[e] && f < e)) ? 1 : 0;
     p.eorder[rank] = e;
     const int m64 = sPad[e + 1] - sPad[e];
-    for (int i = 0; i * BM < m64 && sTiles[e] + i < p.n_mt_max; ++i) {
+    const int tile_rows = p.pair ? 2 * BM : BM;
+    for (int i = 0; i * tile_rows < m64 && sTiles[e] + i < p.n_mt_max; ++i) {
       int* r = p.mtiles + 4 * (sTiles[e] + i);
       r[0] = e;
-      r[1] = sPad[e] + i * BM;
-      r[2] = min(BM, m64 - i * BM);
-      r[3] = 0;
+      r[1] = sPad[e] + i * tile_rows;
+      r[2] = min(BM, m64 - i * tile_rows);
+      r[3] = p.pair ? max(0, min(BM, m64 - i * tile_rows - BM)) : 0;
     }
   }
 }
@@ -241,48 +250,62 @@ struct BUnit {
   int kind, e, m, n, a_row, rows, k0, nk1, nk2;
 };
 
+// Units: one per CTA, or with CTA pairs one per pair (the pair's two CTAs
+// take two 128-row tiles that share the weight tile, each loading half of it).
 __device__ __forceinline__ int bwd_units(const BwdParams& p, int phase) {
   const int n_mt = min(p.meta[BM_NMT], p.n_mt_max);
   const bool sh = p.I_s > 0;
-  if (phase == 0) return n_mt * p.N1 + (sh ? p.n_tt * p.N1s : 0);
-  const int c_e = (p.D / BM) * (p.I / 256) + 2 * (p.I / BM) * (p.D / 256);
-  const int c_s = sh ? (p.D / BM) * (p.I_s / 256) + 2 * (p.I_s / BM) * (p.D / 256) : 0;
-  return c_s + p.E * c_e + n_mt * p.N2 + (sh ? p.n_tt * p.N2 : 0);
+  const int rt = p.pair ? 2 * BM : BM;  // output rows per unit of the weight gradients
+  const int n_tt = p.pair ? (p.n_tt + 1) / 2 : p.n_tt;
+  if (phase == 0) return n_mt * p.N1 + (sh ? n_tt * p.N1s : 0);
+  const int c_e = (p.D / rt) * (p.I / 256) + 2 * (p.I / rt) * (p.D / 256);
+  const int c_s = sh ? (p.D / rt) * (p.I_s / 256) + 2 * (p.I_s / rt) * (p.D / 256) : 0;
+  return c_s + p.E * c_e + n_mt * p.N2 + (sh ? n_tt * p.N2 : 0);
 }
 
 // Phase 0: routed (M-tile, 128 columns of I) units, then the shared expert's
 // (token tile, 128 columns of I_s).  Phase 1: the shared expert's weight
 // gradients (K = T), the routed weight gradients expert by expert in
 // descending route count (K = the expert's padded routes), then dx per route
-// and the shared expert's dx (K = 2I and 2 I_s): longest units first.
-__device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u) {
+// and the shared expert's dx (K = 2I and 2 I_s): longest units first.  With
+// CTA pairs, `rank` picks this CTA's tile of the pair's two (rows = 0: an
+// empty partner, whose A box lies outside its tensor and is zero-filled).
+__device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u, int rank) {
   BUnit b{};
   const int n_mt = min(p.meta[BM_NMT], p.n_mt_max);
+  const int rt = p.pair ? 2 * BM : BM;
+  auto routed_tile = [&](int mt) {
+    b.e = p.mtiles[4 * mt];
+    const int row0 = p.mtiles[4 * mt + 1];
+    b.rows = rank ? p.mtiles[4 * mt + 3] : p.mtiles[4 * mt + 2];
+    b.a_row = b.rows > 0 ? row0 + rank * BM : -2 * BM;
+  };
+  auto shared_tile = [&](int tp) {
+    const int tt = p.pair ? 2 * tp + rank : tp;
+    b.rows = max(0, min(BM, p.T - tt * BM));
+    b.a_row = b.rows > 0 ? tt * BM : -2 * BM;
+  };
   if (phase == 0) {
     const int nr = n_mt * p.N1;
     if (u < nr) {
-      const int mt = u / p.N1;
       b.kind = BU_A_ROUTED;
       b.n = u % p.N1;
-      b.e = p.mtiles[4 * mt];
-      b.a_row = p.mtiles[4 * mt + 1];
-      b.rows = p.mtiles[4 * mt + 2];
+      routed_tile(u / p.N1);
     } else {
-      const int v = u - nr, tt = v / p.N1s;
+      const int v = u - nr;
       b.kind = BU_A_SHARED;
       b.n = v % p.N1s;
-      b.a_row = tt * BM;
-      b.rows = min(BM, p.T - tt * BM);
+      shared_tile(v / p.N1s);
     }
     b.nk1 = b.nk2 = p.D / BK;
     return b;
   }
   const bool sh = p.I_s > 0;
-  const int c_e = (p.D / BM) * (p.I / 256) + 2 * (p.I / BM) * (p.D / 256);
-  const int c_s = sh ? (p.D / BM) * (p.I_s / 256) + 2 * (p.I_s / BM) * (p.D / 256) : 0;
+  const int c_e = (p.D / rt) * (p.I / 256) + 2 * (p.I / rt) * (p.D / 256);
+  const int c_s = sh ? (p.D / rt) * (p.I_s / 256) + 2 * (p.I_s / rt) * (p.D / 256) : 0;
   int v = u;
   if (v < c_s) {  // shared expert weight gradients, K = T
-    const int nd = (p.D / BM) * (p.I_s / 256), nu = (p.I_s / BM) * (p.D / 256);
+    const int nd = (p.D / rt) * (p.I_s / 256), nu = (p.I_s / rt) * (p.D / 256);
     b.nk1 = (p.T + BK - 1) / BK;
     if (v < nd) {
       b.kind = BU_DWS_DOWN;
@@ -295,6 +318,7 @@ __device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u
       b.m = v / (p.D / 256);
       b.n = v % (p.D / 256);
     }
+    if (p.pair) b.m = 2 * b.m + rank;  // in 128-row tiles of the output
     return b;
   }
   v -= c_s;
@@ -303,7 +327,7 @@ __device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u
     v %= c_e;
     b.k0 = p.Sp[b.e];
     b.nk1 = (p.Sp[b.e + 1] - b.k0) / PADK;
-    const int nd = (p.D / BM) * (p.I / 256), nu = (p.I / BM) * (p.D / 256);
+    const int nd = (p.D / rt) * (p.I / 256), nu = (p.I / rt) * (p.D / 256);
     if (v < nd) {
       b.kind = BU_DW_DOWN;
       b.m = v / (p.I / 256);
@@ -315,25 +339,21 @@ __device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u
       b.m = v / (p.D / 256);
       b.n = v % (p.D / 256);
     }
+    if (p.pair) b.m = 2 * b.m + rank;
     return b;
   }
   v -= p.E * c_e;
-  if (v < n_mt * p.N2) {  // dx of the routes of one M-tile
-    const int mt = v / p.N2;
+  if (v < n_mt * p.N2) {  // dx of the routes of one M-tile (pair)
     b.kind = BU_DX_ROUTED;
     b.n = v % p.N2;
-    b.e = p.mtiles[4 * mt];
-    b.a_row = p.mtiles[4 * mt + 1];
-    b.rows = p.mtiles[4 * mt + 2];
+    routed_tile(v / p.N2);
     b.nk1 = b.nk2 = p.I / BK;
     return b;
   }
   v -= n_mt * p.N2;
-  const int tt = v / p.N2;  // the shared expert's dx
-  b.kind = BU_DX_SHARED;
+  b.kind = BU_DX_SHARED;  // the shared expert's dx
   b.n = v % p.N2;
-  b.a_row = tt * BM;
-  b.rows = min(BM, p.T - tt * BM);
+  shared_tile(v / p.N2);
   b.nk1 = b.nk2 = p.I_s / BK;
   return b;
 }
@@ -344,11 +364,27 @@ __device__ __forceinline__ int unit_steps(const BUnit& b) {
              : b.nk1;
 }
 
-// TMA loads of K step s of unit b into stage (sa: A, 16 KB; sb: B, 32 KB);
-// returns the bytes the stage's barrier must count.
-__device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams& p, const BUnit& b, int s,
-                                              uint8_t* sa, uint8_t* sb, uint64_t* bar) {
-  auto box = [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1) { tma_load_2d(dst, m, bar, c0, c1); };
+// {64, 64} boxes one CTA loads for K step s of unit b: A is always two (128
+// rows or columns); B is the whole weight tile for one CTA, or this CTA's half
+// of it in a pair.
+__device__ __forceinline__ uint32_t step_boxes(const BUnit& b, int s, bool pair) {
+  const bool dh = (b.kind == BU_A_ROUTED || b.kind == BU_A_SHARED) && s >= b.nk1;  // B: 128 columns of W_down
+  return 2u + (dh ? (pair ? 1u : 2u) : (pair ? 2u : 4u));
+}
+
+// TMA loads of K step s of unit b into stage (sa: A, 16 KB; sb: B, up to
+// 32 KB).  One CTA: every box completes on `bar`.  CTA pairs: every box of
+// both CTAs completes on the even CTA's barrier (`bar_pair`, a cluster
+// address); this CTA loads its own A rows and its half of B -- for the
+// replayed up/gate tile the even CTA the up rows and the odd CTA the gate
+// rows, otherwise the first or second half of the N columns.
+template <bool kPair>
+__device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p, const BUnit& b, int s, uint8_t* sa,
+                                          uint8_t* sb, uint64_t* bar, uint32_t bar_pair, int rank) {
+  auto box = [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1) {
+    if constexpr (kPair) tma_load_2d_pair(dst, m, bar_pair, c0, c1);
+    else tma_load_2d(dst, m, bar, c0, c1);
+  };
   switch (b.kind) {
     case BU_A_ROUTED:
     case BU_A_SHARED: {
@@ -361,11 +397,17 @@ __device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams
         const int br = (r ? b.e * p.I : 0) + b.n * BN_UP;
         const CUtensorMap* up = r ? &mp.w_up : &mp.ws_up;
         const CUtensorMap* gt = r ? &mp.w_gate : &mp.ws_gate;
-        box(sb, up, kc, br);
-        box(sb + BOXB, up, kc, br + 64);
-        box(sb + 2 * BOXB, gt, kc, br);
-        box(sb + 3 * BOXB, gt, kc, br + 64);
-        return 6 * BOXB;
+        if (kPair) {
+          const CUtensorMap* w = rank ? gt : up;
+          box(sb, w, kc, br);
+          box(sb + BOXB, w, kc, br + 64);
+        } else {
+          box(sb, up, kc, br);
+          box(sb + BOXB, up, kc, br + 64);
+          box(sb + 2 * BOXB, gt, kc, br);
+          box(sb + 3 * BOXB, gt, kc, br + 64);
+        }
+        return;
       }
       // dh' = dO W_down[e]: A = dO rows (K-major), B = W_down[e] [D, I] MN-major (N = I contiguous)
       const int kc = (s - b.nk1) * BK;
@@ -374,9 +416,13 @@ __device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams
       box(sa + BOXB, a, kc, b.a_row + 64);
       const CUtensorMap* dn = r ? &mp.w_down : &mp.ws_down;
       const int krow = (r ? b.e * p.D : 0) + kc;
-      box(sb, dn, b.n * BN_UP, krow);
-      box(sb + BOXB, dn, b.n * BN_UP + 64, krow);
-      return 4 * BOXB;
+      if (kPair) {
+        box(sb, dn, b.n * BN_UP + 64 * rank, krow);
+      } else {
+        box(sb, dn, b.n * BN_UP, krow);
+        box(sb + BOXB, dn, b.n * BN_UP + 64, krow);
+      }
+      return;
     }
     case BU_DX_ROUTED:
     case BU_DX_SHARED: {  // dx = [da_u da_g] [W_up; W_gate]: A K-major, B [I, D] MN-major (N = D contiguous)
@@ -388,9 +434,9 @@ __device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams
       box(sa + BOXB, a, kc, b.a_row + 64);
       const CUtensorMap* w = r ? (second ? &mp.w_gate : &mp.w_up) : (second ? &mp.ws_gate : &mp.ws_up);
       const int krow = (r ? b.e * p.I : 0) + kc;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) box(sb + q * BOXB, w, b.n * 256 + 64 * q, krow);
-      return 6 * BOXB;
+      const int nq = kPair ? 2 : 4, q0 = kPair ? 2 * rank : 0;
+      for (int q = 0; q < nq; ++q) box(sb + q * BOXB, w, b.n * 256 + 64 * (q0 + q), krow);
+      return;
     }
     default: {  // weight gradients: A and B MN-major, K = routes (or tokens)
       const CUtensorMap *a, *bm;
@@ -405,9 +451,9 @@ __device__ __forceinline__ uint32_t bwd_issue(const BwdMaps& mp, const BwdParams
       const int krow = b.k0 + s * BK;
       box(sa, a, b.m * BM, krow);
       box(sa + BOXB, a, b.m * BM + 64, krow);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) box(sb + q * BOXB, bm, b.n * 256 + 64 * q, krow);
-      return 6 * BOXB;
+      const int nq = kPair ? 2 : 4, q0 = kPair ? 2 * rank : 0;
+      for (int q = 0; q < nq; ++q) box(sb + q * BOXB, bm, b.n * 256 + 64 * (q0 + q), krow);
+      return;
     }
   }
 }
@@ -473,164 +519,215 @@ __device__ __forceinline__ float epi_act_grad(uint32_t taddr, float g, bool stor
 }
 
 // ------------------------------------------------------------------ the GEMM kernel
-// Persistent, one CTA per SM, units claimed from a global counter.  Warp 0:
-// TMA producer (claims the units and hands them to the others through a
-// queue in shared memory); warp 1: tcgen05.mma issuer; warps 2-5: epilogue
+// Persistent, one CTA (or one CTA pair) per SM (pair), units claimed from a
+// global counter.  Warp 0: TMA producer (the only or even CTA claims the units
+// and hands them to its other warps, and to the odd CTA, through a queue in
+// shared memory); warp 1: tcgen05.mma issuer (the even CTA issues for both CTAs
+// of a pair, cta_group::2, M = 256); warps 2-5: epilogue of this CTA's 128 rows
 // (TMEM lanes 32 (warp % 4) ...).  Phase 0 keeps one 384-column accumulator
-// (up, gate, dh'); phase 1 alternates two 256-column accumulators.
-template <int PHASE>
+// (up, gate, dh'); phase 1 alternates two 256-column accumulators.  The pair
+// protocol (loads of both CTAs counted on the even CTA's full barrier, MMA
+// commits multicast to both, accumulators handed back by remote arrivals) is
+// the forward kernel's.
+template <int PHASE, bool kPair>
 __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant__ BwdMaps mp, const BwdParams p) {
+  constexpr int NST = kPair ? BWD_PAIR_STAGES : BWD_STAGES;
+  constexpr int STG = kPair ? BWD_PAIR_STAGE : BWD_STAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BWD_STAGES * BWD_STAGE);
-  uint64_t* full = bars;                      // [BWD_STAGES]
-  uint64_t* empty = bars + BWD_STAGES;        // [BWD_STAGES]
-  uint64_t* tfull = bars + 2 * BWD_STAGES;    // [2]
-  uint64_t* tempty = tfull + 2;               // [2]
-  uint64_t* qfull = tempty + 2;               // [BWD_QN]
-  uint64_t* qempty = qfull + BWD_QN;          // [BWD_QN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NST * STG);
+  uint64_t* full = bars;                 // [NST]
+  uint64_t* empty = bars + NST;          // [NST]
+  uint64_t* tfull = bars + 2 * NST;      // [2]
+  uint64_t* tempty = tfull + 2;          // [2]
+  uint64_t* qfull = tempty + 2;          // [BWD_QN]
+  uint64_t* qempty = qfull + BWD_QN;     // [BWD_QN]
   uint64_t* drain = qempty + BWD_QN;
   volatile int* qslot = reinterpret_cast<volatile int*>(drain + 1);  // [BWD_QN]
   volatile int* s_unit = qslot + BWD_QN;
   volatile int* s_ok = s_unit + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(s_ok + 1));
-  static_assert((2 * BWD_STAGES + 4 + 2 * BWD_QN + 1) * 8 + (BWD_QN + 3) * 4 <= 512, "barrier area");
+  static_assert((2 * NST + 4 + 2 * BWD_QN + 1) * 8 + (BWD_QN + 3) * 4 <= BWD_BAR_BYTES, "barrier area");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = kPair ? (int)(cluster_ctarank() & 1u) : 0;
+  const bool leader = rank == 0;
   const int n_units = bwd_units(p, PHASE);
   int* claim_ctr = p.counters + PHASE;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < BWD_STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], kPair ? 8 : 128);  // pairs: one arrival per epilogue warp of both CTAs
     }
     for (int i = 0; i < BWD_QN; ++i) {
       mbar_init(&qfull[i], 1);
-      mbar_init(&qempty[i], 2);
+      mbar_init(&qempty[i], kPair ? 4 : 2);  // MMA issuer + epilogue (pairs: + the odd CTA's producer and epilogue)
     }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc<512>(tmem_slot);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair<512>(tmem_slot);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc<512>(tmem_slot);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the other CTA's barriers exist before anything targets them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // waits on barriers that the other CTA of a pair helps complete
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+    if constexpr (kPair) return mbar_wait_cluster(bar, parity, p.status, p.timeout_ns);
+    else return mbar_wait(bar, parity, p.status, p.timeout_ns);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint32_t full_even = kPair ? mapa_shared(full, 0) : 0u;
+      const uint32_t q_odd = kPair ? mapa_shared(const_cast<int*>(qslot), 1) : 0u;
+      const uint32_t qfull_odd = kPair ? mapa_shared(qfull, 1) : 0u;
+      const uint32_t qempty_even = kPair ? mapa_shared(qempty, 0) : 0u;
       uint32_t stage = 0, phase = 0;
       int issued = 0;
-      int claim = atomicAdd(claim_ctr, 1);
+      int claim = leader ? atomicAdd(claim_ctr, 1) : 0;
       for (int i = 0;; ++i) {
         const int slot = i % BWD_QN;
-        if (!mbar_wait(&qempty[slot], ((uint32_t)(i / BWD_QN) & 1u) ^ 1u, p.status, p.timeout_ns)) break;
-        const int u = claim < n_units ? claim : -1;
-        qslot[slot] = u;
-        mbar_arrive(&qfull[slot]);
+        const uint32_t qpar = (uint32_t)(i / BWD_QN) & 1u;
+        int u = -2;  // -2: a wait ran out; -1: no units left
+        if (leader) {  // publish the claimed unit, then claim the one after it
+          if (wait_bar(&qempty[slot], qpar ^ 1u)) {
+            u = claim < n_units ? claim : -1;
+            qslot[slot] = u;
+            if constexpr (kPair) {
+              st_shared_cluster_u32(q_odd + 4u * slot, (uint32_t)u);
+              mbar_arrive_remote_cluster(qfull_odd + 8u * slot);
+            }
+            mbar_arrive(&qfull[slot]);
+            if (u >= 0) claim = atomicAdd(claim_ctr, 1);
+          }
+        } else if (wait_bar(&qfull[slot], qpar)) {  // odd CTA: the even CTA's unit
+          u = qslot[slot];
+        }
+        if (kPair && !leader && u != -2) mbar_arrive_remote(qempty_even + 8u * slot);
         if (u < 0) break;
-        claim = atomicAdd(claim_ctr, 1);
-        const BUnit b = bwd_decode(p, PHASE, u);
+        const BUnit b = bwd_decode(p, PHASE, u, rank);
         const int ns = unit_steps(b);
         bool ok = true;
         for (int s = 0; s < ns; ++s) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, p.timeout_ns)) { ok = false; break; }
-          uint8_t* sa = smem + stage * BWD_STAGE;
-          // the byte count first: a box may complete before the count is set otherwise
-          const bool dh_step = (b.kind == BU_A_ROUTED || b.kind == BU_A_SHARED) && s >= b.nk1;
-          mbar_arrive_expect_tx(&full[stage], dh_step ? 4u * BOXB : 6u * BOXB);
-          bwd_issue(mp, p, b, s, sa, sa + 2 * BOXB, &full[stage]);
+          if (!wait_bar(&empty[stage], phase ^ 1u)) { ok = false; break; }
+          uint8_t* sa = smem + stage * STG;
+          // the byte count first (pairs: both CTAs' boxes, on the even CTA's barrier)
+          if (leader) mbar_arrive_expect_tx(&full[stage], (kPair ? 2u : 1u) * step_boxes(b, s, kPair) * BOXB);
+          bwd_issue<kPair>(mp, p, b, s, sa, sa + 2 * BOXB, &full[stage], full_even + stage * 8u, rank);
           ++issued;
-          if (++stage == BWD_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
-      for (int i = (issued > BWD_STAGES ? issued - BWD_STAGES : 0); i < issued; ++i)
-        mbar_wait_drain(&full[i % BWD_STAGES], (uint32_t)(i / BWD_STAGES) & 1u, p.timeout_ns);
+      // the last loads issued have landed before the CTA may leave (pairs: the
+      // even CTA's full barriers count both CTAs' loads, and the odd CTA waits
+      // for the even one at the cluster barrier below)
+      if (leader)
+        for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
+          mbar_wait_drain(&full[i % NST], (uint32_t)(i / NST) & 1u, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (elect_one()) {
+    if (leader && elect_one()) {
+      const uint32_t M = kPair ? 2 * BM : BM;
       uint32_t stage = 0, phase = 0;
       uint32_t uses0 = 0u, uses1 = 0u;  // accumulator buffers' use counts (scalars: no local memory)
       uint32_t alt = 0;
       bool ok = true;
+      auto mma = [&](uint32_t d, uint64_t a, uint64_t bd, uint32_t id, uint32_t acc_flag) {
+        if constexpr (kPair) mma_bf16_pair(d, a, bd, id, acc_flag);
+        else mma_bf16_ss(d, a, bd, id, acc_flag);
+      };
       for (int i = 0; ok; ++i) {
         const int slot = i % BWD_QN;
-        if (!mbar_wait(&qfull[slot], (uint32_t)(i / BWD_QN) & 1u, p.status, p.timeout_ns)) break;
+        if (!wait_bar(&qfull[slot], (uint32_t)(i / BWD_QN) & 1u)) break;
         const int u = qslot[slot];
         mbar_arrive(&qempty[slot]);
         if (u < 0) break;
-        const BUnit b = bwd_decode(p, PHASE, u);
+        const BUnit b = bwd_decode(p, PHASE, u, 0);
         const uint32_t acc = PHASE == 0 ? 0u : alt;
         alt ^= (PHASE == 0 ? 0u : 1u);
-        if (!mbar_wait(&tempty[acc], ((acc ? uses1 : uses0) & 1u) ^ 1u, p.status, p.timeout_ns)) break;
+        if (!wait_bar(&tempty[acc], ((acc ? uses1 : uses0) & 1u) ^ 1u)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256u;
         const int ns = unit_steps(b);
         for (int s = 0; s < ns; ++s) {
-          if (!mbar_wait(&full[stage], phase, p.status, p.timeout_ns)) { ok = false; break; }
+          if (!wait_bar(&full[stage], phase)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * BWD_STAGE);
+          const uint32_t a_addr = smem_u32(smem + stage * STG);
           const uint32_t b_addr = a_addr + 2 * BOXB;
           if (b.kind == BU_A_ROUTED || b.kind == BU_A_SHARED) {
             if (s < b.nk1) {  // up/gate into columns [0, 256)
-              const uint32_t id = idesc_bf16_f32(BM, 256);
+              const uint32_t id = idesc_bf16_f32(M, 256);
 #pragma unroll
               for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), id,
-                            (s | kk) != 0 ? 1u : 0u);
+                mma(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), id,
+                    (s | kk) != 0 ? 1u : 0u);
             } else {  // dh' into columns [256, 384)
-              const uint32_t id = idesc_bf16_f32(BM, BN_UP) | IDESC_B_MN;
+              const uint32_t id = idesc_bf16_f32(M, BN_UP) | IDESC_B_MN;
               const int s2 = s - b.nk1;
 #pragma unroll
               for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                mma_bf16_ss(d + 256u, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_mnmajor_sw128(b_addr + kk * 2048),
-                            id, (s2 | kk) != 0 ? 1u : 0u);
+                mma(d + 256u, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_mnmajor_sw128(b_addr + kk * 2048), id,
+                    (s2 | kk) != 0 ? 1u : 0u);
             }
           } else if (b.kind == BU_DX_ROUTED || b.kind == BU_DX_SHARED) {
-            const uint32_t id = idesc_bf16_f32(BM, 256) | IDESC_B_MN;
+            const uint32_t id = idesc_bf16_f32(M, 256) | IDESC_B_MN;
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              mma_bf16_ss(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_mnmajor_sw128(b_addr + kk * 2048), id,
-                          (s | kk) != 0 ? 1u : 0u);
+              mma(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_mnmajor_sw128(b_addr + kk * 2048), id,
+                  (s | kk) != 0 ? 1u : 0u);
           } else {
-            const uint32_t id = idesc_bf16_f32(BM, 256) | IDESC_A_MN | IDESC_B_MN;
+            const uint32_t id = idesc_bf16_f32(M, 256) | IDESC_A_MN | IDESC_B_MN;
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
-              mma_bf16_ss(d, sdesc_mnmajor_sw128(a_addr + kk * 2048), sdesc_mnmajor_sw128(b_addr + kk * 2048), id,
-                          (s | kk) != 0 ? 1u : 0u);
+              mma(d, sdesc_mnmajor_sw128(a_addr + kk * 2048), sdesc_mnmajor_sw128(b_addr + kk * 2048), id,
+                  (s | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
-          if (++stage == BWD_STAGES) { stage = 0; phase ^= 1u; }
+          if constexpr (kPair) mma_commit_pair(&empty[stage], 0x3);
+          else mma_commit(&empty[stage]);
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);  // (a unit with no K steps only hands the buffer on)
+        // (a unit with no K steps only hands the buffer on)
+        if constexpr (kPair) mma_commit_pair(&tfull[acc], 0x3);
+        else mma_commit(&tfull[acc]);
         if (acc) ++uses1; else ++uses0;
       }
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0, p.timeout_ns);
+      if constexpr (kPair) mma_commit_pair(drain, 0x1);
+      else mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.timeout_ns);  // every MMA issued has completed before TMEM is freed
     }
     __syncwarp();
   } else if (warp >= 2 && warp < 6) {
     const int q = warp & 3;
     const int rloc = q * 32 + lane;  // this thread's tile row (TMEM lane)
-    uint32_t uses0 = 0u, uses1 = 0u;  // accumulator buffers' use counts (scalars: no local memory)
+    const uint32_t tempty_even = kPair ? mapa_shared(tempty, 0) : 0u;
+    const uint32_t qempty_even = kPair ? mapa_shared(qempty, 0) : 0u;
+    uint32_t uses0 = 0u, uses1 = 0u;
     uint32_t alt = 0;
     bool ovf = false;
     for (int i = 0;; ++i) {
       if (threadIdx.x == 64) {  // one thread decides for the four warps
         const int slot = i % BWD_QN;
-        if (mbar_wait(&qfull[slot], (uint32_t)(i / BWD_QN) & 1u, p.status, p.timeout_ns)) {
-          *s_unit = qslot[slot];
-          mbar_arrive(&qempty[slot]);
+        if (wait_bar(&qfull[slot], (uint32_t)(i / BWD_QN) & 1u)) {
+          *s_unit = qslot[slot];  // (the store has the value before the arrive)
+          if (kPair && !leader) mbar_arrive_remote(qempty_even + 8u * slot);
+          else mbar_arrive(&qempty[slot]);
         } else {
           *s_unit = -2;
         }
@@ -638,10 +735,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
       named_bar_sync(1, 128);
       const int u = *s_unit;
       if (u < 0) break;
-      const BUnit b = bwd_decode(p, PHASE, u);
+      const BUnit b = bwd_decode(p, PHASE, u, rank);
       const uint32_t acc = PHASE == 0 ? 0u : alt;
       alt ^= (PHASE == 0 ? 0u : 1u);
-      if (threadIdx.x == 64) *s_ok = mbar_wait(&tfull[acc], (acc ? uses1 : uses0) & 1u, p.status, p.timeout_ns) ? 1 : 0;
+      if (threadIdx.x == 64) *s_ok = wait_bar(&tfull[acc], (acc ? uses1 : uses0) & 1u) ? 1 : 0;
       named_bar_sync(1, 128);
       if (*s_ok == 0) break;
       tc_fence_after();
@@ -651,22 +748,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
         const int prow = b.a_row + rloc;
         const int j = valid ? p.prow_route[prow] : -1;
         const float g = j >= 0 ? p.topk_w[j] : 0.0f;  // padding rows: all zero
-        const size_t o = (size_t)prow * p.I + b.n * BN_UP;
+        const size_t o = valid ? (size_t)prow * p.I + b.n * BN_UP : 0;
         const float dg = epi_act_grad(taddr, g, valid, p.hg + o, p.dau + o, p.dag + o);
         if (j >= 0) p.dgp[(size_t)prow * p.N1 + b.n] = dg;
       } else if (b.kind == BU_A_SHARED) {
         const int t = b.a_row + rloc;
-        const bool valid = t < p.T;
+        const bool valid = rloc < b.rows;
         const size_t o = (size_t)(valid ? t : 0) * p.I_s + b.n * BN_UP;
         epi_act_grad(taddr, 1.0f, valid, p.hs + o, p.dasu + o, p.dasg + o);
       } else if (b.kind == BU_DX_ROUTED || b.kind == BU_DX_SHARED) {
         int srow = -1;  // staging row t kY + slot
-        if (b.kind == BU_DX_ROUTED) {
-          const int j = rloc < b.rows ? p.prow_route[b.a_row + rloc] : -1;
-          if (j >= 0) srow = (j / p.k) * p.kY + (j % p.k);
-        } else {
-          const int t = b.a_row + rloc;
-          if (t < p.T) srow = t * p.kY + p.k;
+        if (rloc < b.rows) {
+          if (b.kind == BU_DX_ROUTED) {
+            const int j = p.prow_route[b.a_row + rloc];
+            if (j >= 0) srow = (j / p.k) * p.kY + (j % p.k);
+          } else {
+            srow = (b.a_row + rloc) * p.kY + p.k;
+          }
         }
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -706,17 +804,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) bwd_gemm(const __grid_constant
           store_bf16x32(row + c, v);
         }
       }
+      // hand the accumulator back (pairs: one arrival per warp on the even CTA's barrier)
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (kPair) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_even + acc * 8u);
+      } else {
+        mbar_arrive(&tempty[acc]);
+      }
       if (acc) ++uses1; else ++uses0;
     }
     if (__any_sync(0xffffffffu, ovf) && lane == 0) atomicOr(p.status + 1, FLAG_STAGING_OVERFLOW);
   }
+  if constexpr (kPair) settle_after_abort(p.status);
   tc_fence_before();
   __syncthreads();
+  // pairs: neither CTA frees TMEM or leaves while the other may still issue
+  // into its TMEM, arrive on its barriers or load into its shared memory
+  if constexpr (kPair) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
@@ -988,6 +1097,7 @@ extern "C" int moe_bwd(const moe_plan* pl, int64_t T, const void* x, const moe_w
   p.n_mt_max = (int)L.n_mt_max;
   p.Rp_max = (int)L.Rp_max;
   p.n_wc_max = (int)L.n_wc_max;
+  p.pair = c.mma_pair;  // the backward's GEMMs run as CTA pairs when the plan's forward does
   p.timeout_ns = (long long)c.timeout_ms * 1000000LL;
   p.topk_idx = fv.topk_idx;
   p.topk_w = fv.topk_w;
@@ -1056,19 +1166,40 @@ extern "C" int moe_bwd(const moe_plan* pl, int64_t T, const void* x, const moe_w
 
   cudaStream_t st = (cudaStream_t)stream_;
   const int sms = pl->num_sms;
-  if (cudaFuncSetAttribute(bwd_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(bwd_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM) != cudaSuccess)
+  const bool pair = p.pair != 0;
+  const void* g0 = pair ? reinterpret_cast<const void*>(bwd_gemm<0, true>) : reinterpret_cast<const void*>(bwd_gemm<0, false>);
+  const void* g1 = pair ? reinterpret_cast<const void*>(bwd_gemm<1, true>) : reinterpret_cast<const void*>(bwd_gemm<1, false>);
+  const int gsmem = pair ? BWD_PAIR_SMEM : BWD_SMEM;
+  if (cudaFuncSetAttribute(g0, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess ||
+      cudaFuncSetAttribute(g1, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess)
     return MOE_ERR_CUDA;
+  // one CTA per SM; pairs: clusters of 2 (the even CTA of each issues the pair's MMAs)
+  cudaLaunchConfig_t gcfg = {};
+  gcfg.gridDim = dim3((unsigned)(pair ? (sms & ~1) : sms));
+  gcfg.blockDim = dim3(BWD_THREADS);
+  gcfg.dynamicSmemBytes = gsmem;
+  gcfg.stream = st;
+  cudaLaunchAttribute gattr[1];
+  gattr[0].id = cudaLaunchAttributeClusterDimension;
+  gattr[0].val.clusterDim.x = 2;
+  gattr[0].val.clusterDim.y = 1;
+  gattr[0].val.clusterDim.z = 1;
+  gcfg.attrs = gattr;
+  gcfg.numAttrs = pair ? 1 : 0;
+  auto gemm = [&](int phase) {
+    if (pair) return phase ? cudaLaunchKernelEx(&gcfg, bwd_gemm<1, true>, mp, p) : cudaLaunchKernelEx(&gcfg, bwd_gemm<0, true>, mp, p);
+    return phase ? cudaLaunchKernelEx(&gcfg, bwd_gemm<1, false>, mp, p) : cudaLaunchKernelEx(&gcfg, bwd_gemm<0, false>, mp, p);
+  };
   const int tok_blocks = (int)((T + 7) / 8);  // 8 warps per block, one token per warp
   auto mark = [&](int i) { return !pl->bwd_timed || cudaEventRecord(pl->bwd_timing[i], st) == cudaSuccess; };
   bool ok = mark(0);
   bwd_prep<<<1, 512, 0, st>>>(p);
   bwd_gather<<<4 * sms, 256, 0, st>>>(p);
   ok = ok && mark(1);
-  bwd_gemm<0><<<sms, BWD_THREADS, BWD_SMEM, st>>>(mp, p);
+  ok = ok && gemm(0) == cudaSuccess;
   ok = ok && mark(2);
   bwd_router_dl<<<tok_blocks, 256, 0, st>>>(p);
-  bwd_gemm<1><<<sms, BWD_THREADS, BWD_SMEM, st>>>(mp, p);
+  ok = ok && gemm(1) == cudaSuccess;
   ok = ok && mark(3);
   bwd_router_wr<<<(unsigned)L.n_wc_max, 256, 0, st>>>(p);
   bwd_router_fin<<<(unsigned)c.E, 256, 0, st>>>(p);

@@ -123,36 +123,45 @@ def small(T, D, I, E, k, I_s, score="sigmoid", cid=700, beta=0.3):
     return inp, mi.grad_out(shape)
 
 
+ONE_CTA = dict(minibatch=1024, ring_slots=2, gather_ctas=2)
+PAIRS = dict(minibatch=1024, ring_slots=2, gather_ctas=2, mma_pair=1)  # the backward's GEMMs as CTA pairs too
+
+
+@pytest.mark.parametrize("kw", [ONE_CTA, PAIRS], ids=["one_cta", "pairs"])
 @pytest.mark.parametrize("T", [1, 300])
-def test_backward_small_sigmoid_shared(T):
+def test_backward_small_sigmoid_shared(T, kw):
     inp, dO = small(300, 256, 256, 8, 3, 256)
     inp.x = inp.x[:T].copy()
     inp.T = T
     dO = dO[:T]
-    _, gpu, _ = run_bwd(inp, dO)
+    _, gpu, _ = run_bwd(inp, dO, plan_kw=kw)
     ref = ob.moe_bwd(oracle_params(inp), inp.shape.k, inp.shape.score, f64(dO))
     check_all(gpu, ref)
 
 
-def test_backward_softmax_no_shared_ragged():
+@pytest.mark.parametrize("kw", [ONE_CTA, PAIRS], ids=["one_cta", "pairs"])
+def test_backward_softmax_no_shared_ragged(kw):
     inp, dO = small(333, 512, 256, 16, 4, 0, score="softmax", cid=701, beta=0.0)
-    _, gpu, _ = run_bwd(inp, dO, shared=False)
+    _, gpu, _ = run_bwd(inp, dO, shared=False, plan_kw=kw)
     ref = ob.moe_bwd(oracle_params(inp, shared=False), inp.shape.k, inp.shape.score, f64(dO))
     check_all(gpu, ref)
 
 
-def test_backward_medium_several_tiles():
-    # ragged token tail, several 128-row M-tiles per expert, D and I over many tiles
+@pytest.mark.parametrize("kw", [ONE_CTA, PAIRS], ids=["one_cta", "pairs"])
+def test_backward_medium_several_tiles(kw):
+    # ragged token tail, several 128-row M-tiles per expert (odd counts: empty
+    # partners for pairs), D and I over many tiles
     inp, dO = small(1000, 512, 512, 32, 6, 256, cid=702)
-    _, gpu, _ = run_bwd(inp, dO)
+    _, gpu, _ = run_bwd(inp, dO, plan_kw=kw)
     ref = ob.moe_bwd(oracle_params(inp), inp.shape.k, inp.shape.score, f64(dO))
     check_all(gpu, ref)
 
 
-def test_backward_unrouted_expert_has_zero_gradient():
+@pytest.mark.parametrize("kw", [ONE_CTA, PAIRS], ids=["one_cta", "pairs"])
+def test_backward_unrouted_expert_has_zero_gradient(kw):
     inp, dO = small(256, 256, 256, 8, 2, 0, cid=703)
     inp.b_router[5] = -40.0  # no token selects expert 5
-    _, gpu, res = run_bwd(inp, dO, shared=False)
+    _, gpu, res = run_bwd(inp, dO, shared=False, plan_kw=kw)
     assert res["expert_counts"].cpu().numpy()[5] == 0
     for key in ("dW_up", "dW_gate", "dW_down"):
         assert np.all(npy(gpu[key][5]) == 0.0), key
@@ -162,14 +171,19 @@ def test_backward_unrouted_expert_has_zero_gradient():
 
 
 def test_backward_bitwise_deterministic():
+    """Two calls give the same bits, and the CTA-pair GEMMs give the one-CTA
+    GEMMs' bits (each output element keeps its K order)."""
     import gpu_util
     inp, dO = small(700, 512, 256, 16, 4, 256, cid=704)
     layer = gpu_util.Layer(inp, minibatch=512, ring_slots=2, gather_ctas=2)
     _, a, _ = run_bwd(inp, dO, layer=layer)
     _, b, _ = run_bwd(inp, dO, layer=layer)
+    pl = gpu_util.Layer(inp, weights=layer.w, minibatch=512, ring_slots=2, gather_ctas=2, mma_pair=1)
+    _, c, _ = run_bwd(inp, dO, layer=pl)
     for key in a:
         if a[key] is not None:
             assert torch.equal(a[key], b[key]), key
+            assert torch.equal(a[key], c[key]), f"{key}: pairs differ from one CTA per tile"
 
 
 def test_backward_kimi_k2_full_size_sampled():
