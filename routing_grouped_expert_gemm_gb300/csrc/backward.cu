@@ -322,18 +322,6 @@ __device__ __forceinline__ BUnit bwd_decode(const BwdParams& p, int phase, int u
     return b;
   }
   v -= c_s;
-  // The routed weight-gradient units (expert by expert, descending route
-  // count) and the dx units are interleaved in proportion (a Bresenham walk):
-  // the weight-gradient tiles of small experts (one or two K steps, bound by
-  // their 64 KB of bf16 output stores) then overlap the long, compute-bound dx
-  // tiles instead of running back to back.
-  const int n_w = p.E * c_e;
-  const int n_x = n_mt * p.N2 + (sh ? ((p.pair ? (p.n_tt + 1) / 2 : p.n_tt)) * p.N2 : 0);
-  {
-    const long long nt = (long long)n_w + n_x;
-    const int xa = (int)(((long long)(v + 1) * n_x) / nt), xb = (int)(((long long)v * n_x) / nt);
-    v = xa > xb ? n_w + xb : v - xb;  // a dx unit (the xb-th), else the (v - xb)-th weight unit
-  }
   if (v < p.E * c_e) {  // routed weight gradients of expert eorder[v / c_e]
     b.e = p.eorder[v / c_e];
     v %= c_e;
