@@ -933,6 +933,54 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
                 sfw[d][j] = d < o.nk ? *reinterpret_cast<const uint32_t*>(p.xs + (size_t)tok[j] * (nkg * 4) + d * 4) : 0u;
           }
         }
+        // pairs: one K step's loads into `stage` (lane 0 only), counted on the even CTA's full barrier
+        auto issue_pair = [&](uint32_t stage, int kb) {
+          uint8_t* sa = smem + stage * G::stride;
+          uint8_t* sb = sa + A_STAGE_BYTES;
+          const int kc = kb * (mx ? BK_MX : BK);
+          if (leader)
+            mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(mx ? PAIR_MX_STAGE_TX : PAIR_STAGE_BYTES));
+          const uint32_t fb = full_even + stage * 8u;
+          tma_load_2d_pair(sa, o.a, fb, kc, t.a_row);
+          tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
+          if constexpr (kMxPair) {
+            if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
+              uint8_t* ssf2 = sf_slots + stage * SF_STAGE_BYTES;
+              if (t.kind == TASK_R1) {
+                const int nkg1 = p.D / BK_MX;
+                const int ub = (t.e * p.I + t.n * BN_UP) / BM;
+                tma_load_2d_pair(ssf2, &maps.sf_x, fb, 0, 4 * (t.mt * nkg1 + kb));
+                tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_up, fb, 0, 4 * (ub * nkg1 + kb));
+                tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_gate, fb, 0, 4 * (ub * nkg1 + kb));
+              } else {
+                const int nkg2 = p.I / BK_MX;
+                const int rb = (t.e * p.D + t.n * BN_DOWN) / BM;
+                tma_load_2d_pair(ssf2, &maps.sf_h, fb, 0, 4 * (t.mt * nkg2 + kb));
+                tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * (rb * nkg2 + kb));
+                tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * ((rb + 1) * nkg2 + kb));
+              }
+            }
+          }
+        };
+        if constexpr (kPair) {
+          // pairs gather no rows in the producer: lane 0 alone runs the K steps,
+          // with no warp-wide exchange per step (the single issuing thread's
+          // loop is on the critical path)
+          if (lead_lane) {
+            for (int kb = 0; kb < o.nk; ++kb) {
+              TRACE_T0();
+              if (!wait_bar(&empty[stage], phase ^ 1u)) { ok = false; break; }
+              TRACE_ADD(p, TR_PROD_EMPTY);
+#ifdef MOE_TRACE
+              s_issue_ns[stage] = globaltimer_ns();
+#endif
+              issue_pair(stage, kb);
+              ++issued;
+              if (++stage == NST) { stage = 0; phase ^= 1u; }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        } else {
         for (int kb = 0; kb < o.nk; ++kb) {
           int free = 1;
           if (lead_lane) {
@@ -953,31 +1001,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           if (lead_lane) s_issue_ns[stage] = globaltimer_ns();
 #endif
           if constexpr (kPair) {
-            if (lead_lane) {
-              if (leader)
-                mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(mx ? PAIR_MX_STAGE_TX : PAIR_STAGE_BYTES));
-              const uint32_t fb = full_even + stage * 8u;
-              tma_load_2d_pair(sa, o.a, fb, kc, t.a_row);
-              tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
-              if constexpr (kMxPair) {
-                if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
-                  uint8_t* ssf2 = sf_slots + stage * SF_STAGE_BYTES;
-                  if (t.kind == TASK_R1) {
-                    const int nkg1 = p.D / BK_MX;
-                    const int ub = (t.e * p.I + t.n * BN_UP) / BM;
-                    tma_load_2d_pair(ssf2, &maps.sf_x, fb, 0, 4 * (t.mt * nkg1 + kb));
-                    tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_up, fb, 0, 4 * (ub * nkg1 + kb));
-                    tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_gate, fb, 0, 4 * (ub * nkg1 + kb));
-                  } else {
-                    const int nkg2 = p.I / BK_MX;
-                    const int rb = (t.e * p.D + t.n * BN_DOWN) / BM;
-                    tma_load_2d_pair(ssf2, &maps.sf_h, fb, 0, 4 * (t.mt * nkg2 + kb));
-                    tma_load_2d_pair(ssf2 + SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * (rb * nkg2 + kb));
-                    tma_load_2d_pair(ssf2 + 2 * SF_BLOCK_BYTES, &maps.sf_down, fb, 0, 4 * ((rb + 1) * nkg2 + kb));
-                  }
-                }
-              }
-            }
+            if (lead_lane) issue_pair(stage, kb);
           } else {
             if (gather_a)
               tma_gather4(sa + lane * 4 * 128, &maps.x_rows, &full[stage], kc, tok[0], tok[1], tok[2], tok[3]);
@@ -1039,6 +1063,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           if (lead_lane) DBG_SET(p, DBG_PROD_ISSUED, issued);
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
+        }  // one CTA per tile
       }
       // a cancellation request still in flight is answered before the CTA leaves
       if (lead_lane && clc_pending) mbar_wait_drain(clc_bar, clc_phase, p.timeout_ns);
