@@ -410,7 +410,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   std::memset(&rm, 0, sizeof(rm));
   std::memset(&tm, 0, sizeof(tm));
   const int64_t ring_rows = (int64_t)c.ring_slots * c.minibatch;
-  const uint32_t wr_box = (uint32_t)(p.n_router_cols > 256 ? p.n_router_cols / 2 : p.n_router_cols);
+  const uint32_t wr_box = (uint32_t)(p.n_router_cols > 256 ? p.n_router_cols / 4 : p.n_router_cols / 2);  // per CTA of a pair
   const uint32_t down_box = c.mma_pair ? 128u : (uint32_t)BN_DOWN;  // pairs: each CTA loads half the columns
   int rc = MOE_OK;
   rc |= encode_bf16_2d(pl, &rm.x, x, T, c.D, BM);

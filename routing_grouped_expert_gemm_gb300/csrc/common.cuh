@@ -46,7 +46,7 @@ constexpr int PAIR_MX_STAGE_TX = PAIR_STAGE_BYTES + SF_STAGE_BYTES;  // 33.5 KB
 constexpr int PAIR_MX_STAGES = 6;
 constexpr int ACC_COLS = 256;    // fp32 accumulator columns per tile
 constexpr int MEGA_THREADS = 256;  // 8 warps
-constexpr int ROUTER_THREADS = 192;
+constexpr int ROUTER_THREADS = 256;
 constexpr int SCHED_THREADS = 512;
 constexpr int TOPK_MAX = 16;
 constexpr int E_MAX = 512;

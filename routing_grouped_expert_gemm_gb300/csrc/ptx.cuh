@@ -226,6 +226,11 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem) {
                "r"(kCols)
                : "memory");
 }
+__device__ __forceinline__ void tmem_alloc_pair_dyn(uint32_t* dst_smem, uint32_t cols) {  // whole warp, both CTAs
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(cols)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_relinquish_pair() {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }

@@ -171,7 +171,7 @@ extern "C" int moe_route_static(const moe_plan* pl, int64_t T, const void* x, co
 
   RouterMaps rm;
   std::memset(&rm, 0, sizeof(rm));
-  const uint32_t wr_box = (uint32_t)(p.n_router_cols > 256 ? p.n_router_cols / 2 : p.n_router_cols);
+  const uint32_t wr_box = (uint32_t)(p.n_router_cols > 256 ? p.n_router_cols / 4 : p.n_router_cols / 2);  // per CTA of a pair
   if (encode_rows(pl, &rm.x, x, T, c.D, BM) != MOE_OK || encode_rows(pl, &rm.wr, W_router, c.E, c.D, wr_box) != MOE_OK)
     return MOE_ERR_INVALID_ARG;
   // the router kernel zeroes the status word and the counters; every other
