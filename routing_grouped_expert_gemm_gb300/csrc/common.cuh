@@ -352,9 +352,15 @@ __device__ __forceinline__ float silu_f32(float v) { return v * __fdividef(1.0f,
 // E4M3(v / X) rounded to nearest-even and saturated at +-448; an all-zero block
 // gets the code 0 (X = 2^-127).  Returns the E8M0 code; q receives the codes.
 __device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint32_t* q) {
-  float amax = 0.0f;
+  // max |v| as a pairwise tree (exact in any order; five dependent steps, not 32)
+  float m[16];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+  const float amax = m[0];
   if (amax == 0.0f) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[i] = 0;
@@ -367,14 +373,19 @@ __device__ __forceinline__ uint32_t mx_quantize32(const float* v, uint32_t* q) {
   // v * 2^-se, exact (|result| < 2^9) when 2^-se is a normal float, as ldexpf
   const bool pow2 = se >= -126 && se <= 126;
   const float scale = __uint_as_float((uint32_t)(127 - se) << 23);
+  float a[32];
+  if (pow2) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = v[j] * scale;
+  } else {  // 2^-se is not a normal float (a block of huge or tiny values)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = ldexpf(v[j], -se);
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float a[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a[j] = pow2 ? v[4 * i + j] * scale : ldexpf(v[4 * i + j], -se);
     // two codes per conversion; element 4i + j lands in byte j of the word
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a[0], a[1]), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a[2], a[3]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a[4 * i], a[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a[4 * i + 2], a[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
     q[i] = lo | (hi << 16);
   }
   return (uint32_t)(se + 127);
