@@ -71,6 +71,8 @@ struct BwdMaps {  // every map: 2-D row-major bf16, box {64 columns, 64 rows}, 1
   CUtensorMap x, dO;                     // [T, D]
   CUtensorMap hs, dasu, dasg;            // [T, I_s]
   CUtensorMap ws_up, ws_gate, ws_down;   // [I_s, D], [I_s, D], [D, I_s]
+  // the same tensors read K-major, 128 rows per load: box {64 columns, 128 rows}
+  CUtensorMap k_xg, k_dOg, k_dau, k_dag, k_w_up, k_w_gate, k_x, k_dO, k_dasu, k_dasg, k_ws_up, k_ws_gate;
 };
 
 struct BwdParams {
@@ -391,29 +393,21 @@ __device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p,
       const bool r = b.kind == BU_A_ROUTED;
       if (s < b.nk1) {  // replayed up/gate: A = x rows (K-major), B = [W_up; W_gate] rows (K-major)
         const int kc = s * BK;
-        const CUtensorMap* a = r ? &mp.xg : &mp.x;
-        box(sa, a, kc, b.a_row);
-        box(sa + BOXB, a, kc, b.a_row + 64);
+        box(sa, r ? &mp.k_xg : &mp.k_x, kc, b.a_row);  // 128 rows
         const int br = (r ? b.e * p.I : 0) + b.n * BN_UP;
-        const CUtensorMap* up = r ? &mp.w_up : &mp.ws_up;
-        const CUtensorMap* gt = r ? &mp.w_gate : &mp.ws_gate;
+        const CUtensorMap* up = r ? &mp.k_w_up : &mp.k_ws_up;
+        const CUtensorMap* gt = r ? &mp.k_w_gate : &mp.k_ws_gate;
         if (kPair) {
-          const CUtensorMap* w = rank ? gt : up;
-          box(sb, w, kc, br);
-          box(sb + BOXB, w, kc, br + 64);
+          box(sb, rank ? gt : up, kc, br);
         } else {
           box(sb, up, kc, br);
-          box(sb + BOXB, up, kc, br + 64);
           box(sb + 2 * BOXB, gt, kc, br);
-          box(sb + 3 * BOXB, gt, kc, br + 64);
         }
         return;
       }
       // dh' = dO W_down[e]: A = dO rows (K-major), B = W_down[e] [D, I] MN-major (N = I contiguous)
       const int kc = (s - b.nk1) * BK;
-      const CUtensorMap* a = r ? &mp.dOg : &mp.dO;
-      box(sa, a, kc, b.a_row);
-      box(sa + BOXB, a, kc, b.a_row + 64);
+      box(sa, r ? &mp.k_dOg : &mp.k_dO, kc, b.a_row);
       const CUtensorMap* dn = r ? &mp.w_down : &mp.ws_down;
       const int krow = (r ? b.e * p.D : 0) + kc;
       if (kPair) {
@@ -429,9 +423,7 @@ __device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p,
       const bool r = b.kind == BU_DX_ROUTED;
       const bool second = s >= b.nk1;
       const int kc = (second ? s - b.nk1 : s) * BK;
-      const CUtensorMap* a = r ? (second ? &mp.dag : &mp.dau) : (second ? &mp.dasg : &mp.dasu);
-      box(sa, a, kc, b.a_row);
-      box(sa + BOXB, a, kc, b.a_row + 64);
+      box(sa, r ? (second ? &mp.k_dag : &mp.k_dau) : (second ? &mp.k_dasg : &mp.k_dasu), kc, b.a_row);
       const CUtensorMap* w = r ? (second ? &mp.w_gate : &mp.w_up) : (second ? &mp.ws_gate : &mp.ws_up);
       const int krow = (r ? b.e * p.I : 0) + kc;
       const int nq = kPair ? 2 : 4, q0 = kPair ? 2 * rank : 0;
@@ -1031,10 +1023,11 @@ bool bwd_shape_ok(const moe_config& c) {
   return c.precision == MOE_PREC_BF16 && c.I % 256 == 0 && c.I_s % 256 == 0 && c.D % 256 == 0;
 }
 
-int encode_box64(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols) {
+int encode_box64(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows = 64) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = pl->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1154,6 +1147,14 @@ extern "C" int moe_bwd(const moe_plan* pl, int64_t T, const void* x, const moe_w
   rc |= encode_box64(pl, &mp.w_down, w->W_down, E * D, I);
   rc |= encode_box64(pl, &mp.x, x, (uint64_t)T, D);
   rc |= encode_box64(pl, &mp.dO, dO, (uint64_t)T, D);
+  rc |= encode_box64(pl, &mp.k_xg, p.xg, Rp, D, 128);
+  rc |= encode_box64(pl, &mp.k_dOg, p.dOg, Rp, D, 128);
+  rc |= encode_box64(pl, &mp.k_dau, p.dau, Rp, I, 128);
+  rc |= encode_box64(pl, &mp.k_dag, p.dag, Rp, I, 128);
+  rc |= encode_box64(pl, &mp.k_w_up, w->W_up, E * I, D, 128);
+  rc |= encode_box64(pl, &mp.k_w_gate, w->W_gate, E * I, D, 128);
+  rc |= encode_box64(pl, &mp.k_x, x, (uint64_t)T, D, 128);
+  rc |= encode_box64(pl, &mp.k_dO, dO, (uint64_t)T, D, 128);
   if (shared) {
     rc |= encode_box64(pl, &mp.hs, p.hs, (uint64_t)T, Is);
     rc |= encode_box64(pl, &mp.dasu, p.dasu, (uint64_t)T, Is);
@@ -1161,6 +1162,10 @@ extern "C" int moe_bwd(const moe_plan* pl, int64_t T, const void* x, const moe_w
     rc |= encode_box64(pl, &mp.ws_up, w->Ws_up, Is, D);
     rc |= encode_box64(pl, &mp.ws_gate, w->Ws_gate, Is, D);
     rc |= encode_box64(pl, &mp.ws_down, w->Ws_down, D, Is);
+    rc |= encode_box64(pl, &mp.k_dasu, p.dasu, (uint64_t)T, Is, 128);
+    rc |= encode_box64(pl, &mp.k_dasg, p.dasg, (uint64_t)T, Is, 128);
+    rc |= encode_box64(pl, &mp.k_ws_up, w->Ws_up, Is, D, 128);
+    rc |= encode_box64(pl, &mp.k_ws_gate, w->Ws_gate, Is, D, 128);
   }
   if (rc != MOE_OK) return MOE_ERR_INVALID_ARG;
 
