@@ -77,6 +77,18 @@ int moe_testing_pair_mx_tile(const void* A, const void* B, const void* sf, float
 int moe_testing_mn_tile(const void* A, const void* B, float* D, int N, int a_mn, int b_mn, int lbo, int sbo,
                         void* stream);
 
+/*
+ * One TMA load through a 3-D view (64 columns, row, 64-column block; the
+ * block stride 128 bytes, below the row stride) of src, a device bf16
+ * [rows, cols] row-major matrix (cols a multiple of 128): box {64, 64, 2} at
+ * rows [r0, r0 + 64), column blocks b0 and b0 + 1, 128-byte swizzle, copied
+ * from shared memory to out (device, 16384 bytes) as it landed.  status
+ * (device int): 1 when the load completed, 2 when the wait ran out (200 ms).
+ * Asynchronous on `stream`.  Returns 0, -1 (bad argument), -4 (CUDA error)
+ * or -5 (the tensor-map encoder rejected the view).
+ */
+int moe_testing_tma3d_load(const void* src, int rows, int cols, int r0, int b0, void* out, int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -142,6 +142,8 @@ def testing_lib():
     L.moe_testing_mn_tile.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, vp]
     L.moe_testing_mn_tile.restype = ctypes.c_int
+    L.moe_testing_tma3d_load.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+    L.moe_testing_tma3d_load.restype = ctypes.c_int
     _testing_lib = L
     return L
 

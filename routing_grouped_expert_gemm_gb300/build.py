@@ -27,7 +27,7 @@ TESTING_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_testing.so")
 TRACE_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_trace.so")
 DEBUG_LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300_dbg.so")
 SOURCES = ["api.cu", "router.cu", "schedule.cu", "megakernel.cu", "mxfp8.cu", "route_static.cu", "backward.cu"]
-TESTING_SOURCES = ["probe_mx.cu", "probe_pair.cu", "probe_mn.cu"]
+TESTING_SOURCES = ["probe_mx.cu", "probe_pair.cu", "probe_mn.cu", "probe_tma3d.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

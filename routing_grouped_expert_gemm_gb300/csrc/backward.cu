@@ -73,6 +73,10 @@ struct BwdMaps {  // every map: 2-D row-major bf16, box {64 columns, 64 rows}, 1
   CUtensorMap ws_up, ws_gate, ws_down;   // [I_s, D], [I_s, D], [D, I_s]
   // the same tensors read K-major, 128 rows per load: box {64 columns, 128 rows}
   CUtensorMap k_xg, k_dOg, k_dau, k_dag, k_w_up, k_w_gate, k_x, k_dO, k_dasu, k_dasg, k_ws_up, k_ws_gate;
+  // ... and read MN-major, two 64-column blocks per load: a 3-D view (64 columns,
+  // row, 64-column block; the block stride 128 bytes), box {64, 64, 2}
+  CUtensorMap m_xg, m_dOg, m_hg, m_dau, m_dag, m_w_up, m_w_gate, m_w_down;
+  CUtensorMap m_x, m_dO, m_hs, m_dasu, m_dasg, m_ws_up, m_ws_gate, m_ws_down;
 };
 
 struct BwdParams {
@@ -81,6 +85,7 @@ struct BwdParams {
   int n_tt;               // token tiles ceil(T/128)
   int n_mt_max, Rp_max, n_wc_max;
   int pair;               // 1: CTA pairs (cta_group::2); M-tile entries are pairs of tiles
+  int mn3d;               // 1: the 3-D MN-major maps are encoded (two 64-column blocks per load)
   long long timeout_ns;
   // the forward's routing and schedule (its workspace)
   const int* topk_idx;
@@ -387,6 +392,17 @@ __device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p,
     if constexpr (kPair) tma_load_2d_pair(dst, m, bar_pair, c0, c1);
     else tma_load_2d(dst, m, bar, c0, c1);
   };
+  // MN-major columns [col, col + 128) of K rows [krow, krow + 64): one 3-D load,
+  // or two {64, 64} boxes
+  auto mn128 = [&](uint8_t* dst, const CUtensorMap* m2, const CUtensorMap* m3, int col, int krow) {
+    if (p.mn3d) {
+      if constexpr (kPair) tma_load_3d_pair(dst, m3, bar_pair, 0, krow, col / 64);
+      else tma_load_3d(dst, m3, bar, 0, krow, col / 64);
+    } else {
+      box(dst, m2, col, krow);
+      box(dst + BOXB, m2, col + 64, krow);
+    }
+  };
   switch (b.kind) {
     case BU_A_ROUTED:
     case BU_A_SHARED: {
@@ -413,8 +429,7 @@ __device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p,
       if (kPair) {
         box(sb, dn, b.n * BN_UP + 64 * rank, krow);
       } else {
-        box(sb, dn, b.n * BN_UP, krow);
-        box(sb + BOXB, dn, b.n * BN_UP + 64, krow);
+        mn128(sb, dn, r ? &mp.m_w_down : &mp.m_ws_down, b.n * BN_UP, krow);
       }
       return;
     }
@@ -425,26 +440,26 @@ __device__ __forceinline__ void bwd_issue(const BwdMaps& mp, const BwdParams& p,
       const int kc = (second ? s - b.nk1 : s) * BK;
       box(sa, r ? (second ? &mp.k_dag : &mp.k_dau) : (second ? &mp.k_dasg : &mp.k_dasu), kc, b.a_row);
       const CUtensorMap* w = r ? (second ? &mp.w_gate : &mp.w_up) : (second ? &mp.ws_gate : &mp.ws_up);
+      const CUtensorMap* w3 = r ? (second ? &mp.m_w_gate : &mp.m_w_up) : (second ? &mp.m_ws_gate : &mp.m_ws_up);
       const int krow = (r ? b.e * p.I : 0) + kc;
-      const int nq = kPair ? 2 : 4, q0 = kPair ? 2 * rank : 0;
-      for (int q = 0; q < nq; ++q) box(sb + q * BOXB, w, b.n * 256 + 64 * (q0 + q), krow);
+      const int nq = kPair ? 1 : 2, q0 = kPair ? rank : 0;  // 128-column halves
+      for (int q = 0; q < nq; ++q) mn128(sb + 2 * q * BOXB, w, w3, b.n * 256 + 128 * (q0 + q), krow);
       return;
     }
     default: {  // weight gradients: A and B MN-major, K = routes (or tokens)
-      const CUtensorMap *a, *bm;
+      const CUtensorMap *a, *bm, *a3, *bm3;
       switch (b.kind) {
-        case BU_DW_DOWN: a = &mp.dOg; bm = &mp.hg; break;
-        case BU_DW_UP: a = &mp.dau; bm = &mp.xg; break;
-        case BU_DW_GATE: a = &mp.dag; bm = &mp.xg; break;
-        case BU_DWS_DOWN: a = &mp.dO; bm = &mp.hs; break;
-        case BU_DWS_UP: a = &mp.dasu; bm = &mp.x; break;
-        default: a = &mp.dasg; bm = &mp.x; break;
+        case BU_DW_DOWN: a = &mp.dOg; bm = &mp.hg; a3 = &mp.m_dOg; bm3 = &mp.m_hg; break;
+        case BU_DW_UP: a = &mp.dau; bm = &mp.xg; a3 = &mp.m_dau; bm3 = &mp.m_xg; break;
+        case BU_DW_GATE: a = &mp.dag; bm = &mp.xg; a3 = &mp.m_dag; bm3 = &mp.m_xg; break;
+        case BU_DWS_DOWN: a = &mp.dO; bm = &mp.hs; a3 = &mp.m_dO; bm3 = &mp.m_hs; break;
+        case BU_DWS_UP: a = &mp.dasu; bm = &mp.x; a3 = &mp.m_dasu; bm3 = &mp.m_x; break;
+        default: a = &mp.dasg; bm = &mp.x; a3 = &mp.m_dasg; bm3 = &mp.m_x; break;
       }
       const int krow = b.k0 + s * BK;
-      box(sa, a, b.m * BM, krow);
-      box(sa + BOXB, a, b.m * BM + 64, krow);
-      const int nq = kPair ? 2 : 4, q0 = kPair ? 2 * rank : 0;
-      for (int q = 0; q < nq; ++q) box(sb + q * BOXB, bm, b.n * 256 + 64 * (q0 + q), krow);
+      mn128(sa, a, a3, b.m * BM, krow);
+      const int nq = kPair ? 1 : 2, q0 = kPair ? rank : 0;  // 128-column halves
+      for (int q = 0; q < nq; ++q) mn128(sb + 2 * q * BOXB, bm, bm3, b.n * 256 + 128 * (q0 + q), krow);
       return;
     }
   }
@@ -1035,6 +1050,19 @@ int encode_box64(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t r
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
+// 3-D view of a row-major bf16 [rows, cols] matrix for MN-major loads: (64
+// columns, row, 64-column block), box {64, 64, 2}
+int encode_mn3d(const moe_plan* pl, CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols) {
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = pl->encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -1168,6 +1196,27 @@ extern "C" int moe_bwd(const moe_plan* pl, int64_t T, const void* x, const moe_w
     rc |= encode_box64(pl, &mp.k_ws_gate, w->Ws_gate, Is, D, 128);
   }
   if (rc != MOE_OK) return MOE_ERR_INVALID_ARG;
+  // the MN-major 3-D views (without them every MN-major tile is two 2-D loads)
+  int rc3 = MOE_OK;
+  rc3 |= encode_mn3d(pl, &mp.m_xg, p.xg, Rp, D);
+  rc3 |= encode_mn3d(pl, &mp.m_dOg, p.dOg, Rp, D);
+  rc3 |= encode_mn3d(pl, &mp.m_hg, p.hg, Rp, I);
+  rc3 |= encode_mn3d(pl, &mp.m_dau, p.dau, Rp, I);
+  rc3 |= encode_mn3d(pl, &mp.m_dag, p.dag, Rp, I);
+  rc3 |= encode_mn3d(pl, &mp.m_w_up, w->W_up, E * I, D);
+  rc3 |= encode_mn3d(pl, &mp.m_w_gate, w->W_gate, E * I, D);
+  rc3 |= encode_mn3d(pl, &mp.m_w_down, w->W_down, E * D, I);
+  rc3 |= encode_mn3d(pl, &mp.m_x, x, (uint64_t)T, D);
+  rc3 |= encode_mn3d(pl, &mp.m_dO, dO, (uint64_t)T, D);
+  if (shared) {
+    rc3 |= encode_mn3d(pl, &mp.m_hs, p.hs, (uint64_t)T, Is);
+    rc3 |= encode_mn3d(pl, &mp.m_dasu, p.dasu, (uint64_t)T, Is);
+    rc3 |= encode_mn3d(pl, &mp.m_dasg, p.dasg, (uint64_t)T, Is);
+    rc3 |= encode_mn3d(pl, &mp.m_ws_up, w->Ws_up, Is, D);
+    rc3 |= encode_mn3d(pl, &mp.m_ws_gate, w->Ws_gate, Is, D);
+    rc3 |= encode_mn3d(pl, &mp.m_ws_down, w->Ws_down, D, Is);
+  }
+  p.mn3d = rc3 == MOE_OK ? 1 : 0;
 
   cudaStream_t st = (cudaStream_t)stream_;
   const int sms = pl->num_sms;
