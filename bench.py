@@ -62,10 +62,9 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the minibatch sweep (512 / 2048 / 8192 / 32768 and ring vs over-allocation)")
     ap.add_argument("--gather-ctas-mx", type=int, default=6, help="gather CTAs for the MXFP8 layer")
-    ap.add_argument("--dispatch", choices=["ring", "direct", "spread"], default=None,
-                    help="BF16 layer: how the routed tokens reach the expert tiles (default: ring with "
-                         "--gather-ctas gather CTAs on the DeepSeek-V3 shape, spread on the others, the "
-                         "faster of the two measured on each)")
+    ap.add_argument("--dispatch", choices=["ring", "direct", "spread"], default="spread",
+                    help="BF16 layer: how the routed tokens reach the expert tiles (spread: every GEMM CTA "
+                         "fills the ring, measured fastest on every workload; ring: --gather-ctas CTAs fill it)")
     ap.add_argument("--dispatch-mx", choices=["ring", "direct", "spread"], default="spread",
                     help="MXFP8 layer: the same choice (spread measured fastest on DSV3)")
     ap.add_argument("--mma-pair", type=int, default=1, choices=[0, 1],
@@ -251,11 +250,7 @@ def workload_config(shape, args):
 
 
 def dispatch_of(shape, args) -> str:
-    if shape.precision == "mxfp8":
-        return args.dispatch_mx
-    if args.dispatch is not None:
-        return args.dispatch
-    return "ring" if shape.name.startswith("dsv3") else "spread"
+    return args.dispatch_mx if shape.precision == "mxfp8" else args.dispatch
 
 
 def l2_note(shape) -> str:

@@ -3,8 +3,8 @@ E = 256, k = 8, one shared expert) through the C ABI, against the fp64 oracle.
 
 BF16 with the Zipf(1.1) expert load, MXFP8 routed experts with the uniform
 load.  For each precision one set of device weights serves every launch
-configuration: the benchmark's (CTA pairs; ring dispatch with 8 gather CTAs
-for BF16, spread for MXFP8), the minibatch sizes 512, 2048 and 32768 that
+configuration: the benchmark's (CTA pairs, spread dispatch), CTA pairs with
+ring dispatch (8 gather CTAs for BF16, 6 for MXFP8), the minibatch sizes 512, 2048 and 32768 that
 "Mixture-of-Kittens: MoE Megakernel for NVL72s" sweeps (Sec. 3.2, Fig. 5;
 32768 x 4 ring slots holds all T*k routes: the over-allocated buffer of
 Sec. 3.3), the one-CTA kernel with each dispatch mode, and the one-CTA kernel
@@ -31,7 +31,8 @@ pytestmark = pytest.mark.gpu
 N_SAMPLE = 1024
 
 BF16_CONFIGS = [  # (name, plan knobs); the first is the benchmark's
-    ("bench", dict(minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("bench", dict(minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)),
+    ("pair_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("b512", dict(minibatch=512, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("b2048", dict(minibatch=2048, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("b32768x4", dict(minibatch=32768, ring_slots=4, gather_ctas=8, mma_pair=1)),
