@@ -115,15 +115,18 @@ __device__ void gather_copy_row_mx(const FwdParams& p, int t, uint8_t* dst_row, 
 __device__ void gather_role_spread(const FwdParams& p, int part, int parts, volatile int* s_gflag) {
   const int w = (threadIdx.x >> 5) - 6;  // 0 or 1
   const bool lead = threadIdx.x == 6 * 32;
+  constexpr int CH = BM / 32;  // 32-row chunks per M-tile
   for (int m = 0; m < p.n_mb; ++m) {
     const int mt0 = p.meta[META_MB + 4 * m + 2], ntile = p.meta[META_MB + 4 * m + 3];
-    // M-tile mt of the run goes to part mt % parts, so that with small
-    // minibatches (few M-tiles each) the fill still rotates over every part.
-    // A part with no M-tile in this minibatch only reports it done: it neither
-    // waits for the ring slot nor writes to it (waiting would make every
-    // minibatch a grid-wide step)
-    const int i0 = ((part - mt0) % parts + parts) % parts;  // this part's first tile of the minibatch
-    const bool mine = i0 < ntile;
+    // The minibatch's M-tiles are filled in 32-row chunks: chunk c of the run
+    // (M-tile c / CH) goes to part c % parts, so that a small minibatch (few
+    // M-tiles) still spreads over many parts and the chunks rotate over every
+    // part.  A part with no chunk in this minibatch only reports it done: it
+    // neither waits for the ring slot nor writes to it (waiting would make
+    // every minibatch a grid-wide step)
+    const int nch = ntile * CH;
+    const int i0 = ((part - mt0 * CH) % parts + parts) % parts;  // this part's first chunk of the minibatch
+    const bool mine = i0 < nch;
     if (mine && m >= p.slots) {  // ring slot m % slots free again: minibatch m - slots' up/gate tiles are done
       if (lead)
         *s_gflag = wait_counter_ge(p.counters + ctr_r1(p, m - p.slots), p.meta[META_MB + 4 * (m - p.slots)],
@@ -133,10 +136,11 @@ __device__ void gather_role_spread(const FwdParams& p, int part, int parts, vola
     }
     const int lo = m * p.b;
     const size_t slot_base = (size_t)(m % p.slots) * p.b;
-    for (int i = i0; i < ntile; i += parts) {
-      const int mt = mt0 + i;
+    for (int i = i0; i < nch; i += parts) {
+      const int mt = mt0 + i / CH;
       const int p0 = p.mtiles[4 * mt + 1], rows = p.mtiles[4 * mt + 2];
-      for (int r = w; r < rows; r += 2) {
+      const int r1 = min(rows, (i % CH + 1) * 32);
+      for (int r = (i % CH) * 32 + w; r < r1; r += 2) {
         const int t = p.sched[(size_t)(p0 + r) * 3];
         const size_t ring_row = slot_base + (size_t)(p0 + r - lo);
         if (p.mx)

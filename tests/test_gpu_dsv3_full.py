@@ -34,6 +34,7 @@ BF16_CONFIGS = [  # (name, plan knobs); the first is the benchmark's
     ("bench", dict(minibatch=8192, ring_slots=4, dispatch="spread", mma_pair=1)),
     ("pair_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("b512", dict(minibatch=512, ring_slots=4, gather_ctas=8, mma_pair=1)),
+    ("b512_spread", dict(minibatch=512, ring_slots=4, dispatch="spread", mma_pair=1)),
     ("b2048", dict(minibatch=2048, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("b32768x4", dict(minibatch=32768, ring_slots=4, gather_ctas=8, mma_pair=1)),
     ("one_cta_ring", dict(minibatch=8192, ring_slots=4, gather_ctas=8)),
