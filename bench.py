@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--mma-pair", type=int, default=1, choices=[0, 1],
                     help="CTA-pair (cta_group::2) expert tiles, BF16 and MXFP8 (measured fastest on DSV3)")
     ap.add_argument("--raster", type=int, default=0, help="up/gate tile order: M-tiles per group (0 = default)")
+    ap.add_argument("--plain-launch", action="store_true",
+                    help="profiling only: launch the persistent kernel without the cooperative attribute, "
+                         "so that ncu can replay the CTA-pair kernel")
     ap.add_argument("--gemm-ctas", type=int, default=0, help="CTAs that run expert tiles (0 = all remaining SMs)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling only: a smaller case with this many tokens (uniform routing)")
@@ -279,12 +282,12 @@ def kernel_sources_hash() -> str:
 
 
 def recorded_traffic(key: str, cfg: dict):
-    """dram__bytes_read.sum + dram__bytes_write.sum of one persistent-kernel
-    launch, from profiles/traffic_<key>.txt, if it was taken from these sources
-    and this launch configuration; else None."""
+    """(dram__bytes_read.sum + dram__bytes_write.sum of one persistent-kernel
+    launch, the record's note) from profiles/traffic_<key>.txt, if it was taken
+    from these sources and this launch configuration; else (None, None)."""
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", f"traffic_{key}.txt")
     if not os.path.exists(path):
-        return None
+        return None, None
     rec = {}
     with open(path) as fh:
         for line in fh:
@@ -292,14 +295,25 @@ def recorded_traffic(key: str, cfg: dict):
             if len(parts) == 2 and not line.startswith("#"):
                 rec[parts[0]] = parts[1].strip()
     if rec.get("sources_sha256") != kernel_sources_hash():
-        return None
+        return None, None
     for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch", "gemm_ctas"):
         if k in rec and str(cfg.get(k)) != rec[k]:
-            return None
+            return None, None
     try:
-        return float(rec["dram_bytes_per_launch"])
+        return float(rec["dram_bytes_per_launch"]), rec.get("note", "")
     except (KeyError, ValueError):
-        return None
+        return None, None
+
+
+def attach_traffic(roof: dict, shape, cfg: dict) -> dict:
+    """The roofline's `traffic`: a recorded ncu figure of these sources and this
+    launch configuration, else null."""
+    key = f"{shape.name}_{shape.precision}"
+    traffic, note = recorded_traffic(key, cfg)
+    roof["traffic"] = traffic
+    roof["traffic_note"] = (f"{note} (profiles/traffic_{key}.txt)" if traffic
+                            else "no ncu capture for these sources and this launch configuration")
+    return roof
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -316,7 +330,7 @@ class Runner:
         plan_kw = dict(minibatch=args.minibatch, ring_slots=args.ring_slots,
                        gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8" else args.gather_ctas,
                        lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
-                       gemm_ctas=args.gemm_ctas, mma_pair=args.mma_pair)
+                       gemm_ctas=args.gemm_ctas, mma_pair=args.mma_pair, plain_launch=int(args.plain_launch))
         plan_kw.update(knobs)
         self.knobs = plan_kw
         self.plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,
@@ -717,12 +731,7 @@ def run_ours(args, world, rank, local):
     flops = shape.flops(T)
     mega_mean = sum(res["mega_ms"]) / len(res["mega_ms"])
     cfg = workload_config(shape, args)
-    roof = tensor_roofline(shape, mega_mean, bf16_peak, peak_src, burst_peak)
-    traffic = recorded_traffic(f"{shape.name}_{shape.precision}", cfg)
-    roof["traffic"] = traffic
-    roof["traffic_note"] = (("DRAM bytes per launch from a small-case ncu capture scaled to this workload "
-                             "(profiles/traffic_%s_%s.txt)" % (shape.name, shape.precision)) if traffic
-                            else "no ncu capture for these sources and this launch configuration")
+    roof = attach_traffic(tensor_roofline(shape, mega_mean, bf16_peak, peak_src, burst_peak), shape, cfg)
     line = {
         "metric": METRIC,
         "value": replica_throughput(world, T, args.steps, elapsed_ms), "unit": "tokens/s", "n_gpus": world,
@@ -781,7 +790,8 @@ def run_ours(args, world, rank, local):
             "config": workload_config(mshape, args),
             "phases_ms_mean": {"router_topk": statistics.mean(mres["router_ms"]),
                                "schedule": statistics.mean(mres["sched_ms"]), "megakernel": m_mega},
-            "roofline": tensor_roofline(mshape, m_mega, bf16_peak, peak_src, burst_peak),
+            "roofline": attach_traffic(tensor_roofline(mshape, m_mega, bf16_peak, peak_src, burst_peak), mshape,
+                                       workload_config(mshape, args)),
             "phase_bandwidth": phase_bandwidths(mshape, mres, hbm_peak),
             "gpu_launches": mrun.launches * args.steps,
             "clocks": mres["clocks"],

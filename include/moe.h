@@ -124,6 +124,14 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              timeout_ms and the forward ends with MOE_STATUS_TIMEOUT (the
  *              kernels return normally, the stream stays usable).  Ring or
  *              spread dispatch only (direct gives MOE_ERR_INVALID_ARG).
+ *   plain_launch  profiling aid, 0 in normal use: 1 launches the persistent
+ *              kernel without the cooperative attribute (profilers that replay
+ *              kernels cannot launch a cooperative cluster kernel).  Its CTAs
+ *              still wait on each other, so the grid (sized to what fits on
+ *              the GPU at once) must all be resident, which it is when nothing
+ *              else runs on the GPU; every wait is bounded, so a grid that
+ *              did not fit ends the forward with MOE_STATUS_TIMEOUT.  Ignored
+ *              with clc (never cooperative).
  *   raster     order of an expert segment's up/gate tiles: groups of `raster`
  *              M-tiles, each group sweeping all I/128 column tiles (so a
  *              group's token rows are re-read from L2 while its weight
@@ -154,6 +162,7 @@ typedef struct moe_config {
   int32_t raster;
   int32_t test_unfilled_minibatch;
   int32_t clc;
+  int32_t plain_launch;
 } moe_config;
 
 /*

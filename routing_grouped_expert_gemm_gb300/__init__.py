@@ -54,7 +54,8 @@ class moe_config(ctypes.Structure):
                 ("gather_ctas", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32), ("lag", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("dispatch", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
                 ("mma_pair", ctypes.c_int32), ("raster", ctypes.c_int32),
-                ("test_unfilled_minibatch", ctypes.c_int32), ("clc", ctypes.c_int32)]
+                ("test_unfilled_minibatch", ctypes.c_int32), ("clc", ctypes.c_int32),
+                ("plain_launch", ctypes.c_int32)]
 
 
 class moe_weights(ctypes.Structure):
@@ -190,7 +191,7 @@ class Plan:
 
 def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
                     ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0, dispatch=MOE_DISPATCH_RING,
-                    l2_prefetch=0, mma_pair=0, raster=0, test_unfilled_minibatch=0, clc=0) -> Plan:
+                    l2_prefetch=0, mma_pair=0, raster=0, test_unfilled_minibatch=0, clc=0, plain_launch=0) -> Plan:
     if isinstance(score_fn, str):
         score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
     if isinstance(precision, str):
@@ -198,7 +199,7 @@ def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precis
     if isinstance(dispatch, str):
         dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT, "spread": MOE_DISPATCH_SPREAD}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
-                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster, test_unfilled_minibatch, clc)
+                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster, test_unfilled_minibatch, clc, plain_launch)
     h = ctypes.c_void_p()
     rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
     if rc != MOE_OK:

@@ -190,6 +190,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   if (c.mma_pair != 0 && c.mma_pair != 1) return MOE_ERR_INVALID_ARG;
   // cluster launch control schedules the one-CTA kernel
   if (c.clc != 0 && c.clc != 1) return MOE_ERR_INVALID_ARG;
+  if (c.plain_launch != 0 && c.plain_launch != 1) return MOE_ERR_INVALID_ARG;
   if (c.clc && c.mma_pair) return MOE_ERR_INVALID_ARG;
 #ifdef MOE_DEBUG_LOG
   if (c.clc) return MOE_ERR_INVALID_ARG;  // the progress records are sized for the persistent grid
@@ -365,6 +366,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.l2_prefetch = c.l2_prefetch;
   p.test_unfilled = c.test_unfilled_minibatch;
   p.clc = c.clc;
+  p.plain_launch = c.plain_launch;
   p.x = static_cast<const bf16*>(x);
   p.b_router = w->b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);

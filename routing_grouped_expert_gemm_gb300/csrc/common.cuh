@@ -94,6 +94,7 @@ struct FwdParams {
   int mx;               // routed experts in MXFP8 (1) or BF16 (0)
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
   int pair;             // 1: GEMM CTAs run as pairs, tasks 2i and 2i + 1 share one cta_group::2 MMA
+  int plain_launch;     // 1: the persistent kernel is launched without the cooperative attribute (profiling)
   int spread;           // 1: two spare warps of every GEMM CTA fill the ring (no gather CTAs)
   int gparts;           // parts the ring fill of a minibatch is split into (gather CTAs or GEMM CTAs)
   int raster;           // M-tiles per group of a segment's up/gate tiles (column tiles swept per group)

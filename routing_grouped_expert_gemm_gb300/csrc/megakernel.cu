@@ -1392,8 +1392,11 @@ cudaError_t launch_megakernel(const TensorMaps& maps, const FwdParams& p, int gr
   attr[1].val.clusterDim.x = 2;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pair ? 2 : (p.clc ? 0 : 1);  // cluster launch control: not cooperative (the grid exceeds the SMs)
+  // cluster launch control: not cooperative (the grid exceeds the SMs); the
+  // profiling launch: not cooperative either (the grid still fits the GPU)
+  const bool coop = !p.clc && !p.plain_launch;
+  cfg.attrs = coop ? attr : attr + 1;
+  cfg.numAttrs = (coop ? 1 : 0) + (pair ? 1 : 0);
   if (pair_mx) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair_mx, maps, p);
   if (pair) return cudaLaunchKernelEx(&cfg, moe_megakernel_pair, maps, p);
   return cudaLaunchKernelEx(&cfg, moe_megakernel, maps, p);

@@ -73,6 +73,25 @@ def test_pair_bitwise_deterministic_across_knobs():
         assert np.array_equal(o, outs[0][1]), f"output bits differ for {kw}"
 
 
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+def test_pair_plain_launch_is_bitwise_identical(precision):
+    """The profiling launch (no cooperative attribute; the grid still fits the
+    GPU) gives the bits of the cooperative launch."""
+    import gpu_util as g
+    inp = small(1000, 512, 256, 32, 6, 256, cid=313)
+    if precision == "mxfp8":
+        inp = mi.make_inputs(mi.custom_shape(1000, 512, 256, 32, 6, 256, config_id=313, precision="mxfp8"),
+                             calibration={"beta": None, "redraw": {}})
+    x = g.to_dev_bf16(inp.x)
+    outs = []
+    for plain in (0, 1):
+        layer = g.Layer(inp, minibatch=512, ring_slots=3, dispatch="spread", mma_pair=1, plain_launch=plain)
+        res = layer.run(x, poison=True)
+        assert res["status"] == 0
+        outs.append(res["out"].view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_pair_rejects_unsupported_modes():
     import routing_grouped_expert_gemm_gb300 as rg
     for kw in (dict(precision="mxfp8", dispatch="direct"), dict(dispatch="direct"), dict(gather_ctas=3)):
