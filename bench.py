@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--mma-pair", type=int, default=1, choices=[0, 1],
                     help="CTA-pair (cta_group::2) expert tiles, BF16 and MXFP8 (measured fastest on DSV3)")
     ap.add_argument("--raster", type=int, default=0, help="up/gate tile order: M-tiles per group (0 = default)")
+    ap.add_argument("--pad-odd-tiles", type=int, default=0, choices=[0, 1],
+                    help="CTA pairs: 1 runs an expert segment's odd last M-tile with an empty partner instead of "
+                         "splitting it over the pair (bf16; MXFP8 always pads)")
     ap.add_argument("--plain-launch", action="store_true",
                     help="profiling only: launch the persistent kernel without the cooperative attribute, "
                          "so that ncu can replay the CTA-pair kernel")
@@ -246,6 +249,7 @@ def workload_config(shape, args):
            if dispatch_of(shape, args) == "ring" else 0,
            "lag": args.lag, "dispatch": dispatch_of(shape, args),
            "mma_pair": args.mma_pair, "raster": args.raster,
+           "pad_odd_tiles": (args.pad_odd_tiles if shape.precision == "bf16" else 1) if args.mma_pair else None,
            "gemm_ctas": args.gemm_ctas or "all remaining SMs",
            "l2": l2_note(shape),
            "parallelism": "replicas"}
@@ -296,7 +300,8 @@ def recorded_traffic(key: str, cfg: dict):
                 rec[parts[0]] = parts[1].strip()
     if rec.get("sources_sha256") != kernel_sources_hash():
         return None, None
-    for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch", "gemm_ctas"):
+    for k in ("minibatch", "ring_slots", "gather_ctas", "mma_pair", "raster", "dispatch", "pad_odd_tiles",
+              "gemm_ctas"):
         if k in rec and str(cfg.get(k)) != rec[k]:
             return None, None
     try:
@@ -330,7 +335,8 @@ class Runner:
         plan_kw = dict(minibatch=args.minibatch, ring_slots=args.ring_slots,
                        gather_ctas=args.gather_ctas_mx if shape.precision == "mxfp8" else args.gather_ctas,
                        lag=args.lag, dispatch=dispatch_of(shape, args), raster=args.raster,
-                       gemm_ctas=args.gemm_ctas, mma_pair=args.mma_pair, plain_launch=int(args.plain_launch))
+                       gemm_ctas=args.gemm_ctas, mma_pair=args.mma_pair, plain_launch=int(args.plain_launch),
+                       pad_odd_tiles=args.pad_odd_tiles)
         plan_kw.update(knobs)
         self.knobs = plan_kw
         self.plan = rg.moe_plan_create(T, shape.D, shape.I, shape.E, shape.k, shape.I_s, score_fn=shape.score,

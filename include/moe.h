@@ -124,6 +124,12 @@ typedef enum moe_dispatch { MOE_DISPATCH_RING = 0, MOE_DISPATCH_DIRECT = 1, MOE_
  *              timeout_ms and the forward ends with MOE_STATUS_TIMEOUT (the
  *              kernels return normally, the stream stays usable).  Ring or
  *              spread dispatch only (direct gives MOE_ERR_INVALID_ARG).
+ *   pad_odd_tiles  CTA pairs: 1 pairs an expert segment's odd last M-tile with
+ *              an empty partner (one M = 256 MMA, 128 of its rows zero); 0 =
+ *              the default: with bf16 precision the tile is split over the
+ *              pair instead (one M = 128 MMA, 64 rows per CTA: half the A
+ *              bytes and half the tensor time of the padded form).  MXFP8
+ *              pairs always pad.  Results are bitwise the same either way.
  *   plain_launch  profiling aid, 0 in normal use: 1 launches the persistent
  *              kernel without the cooperative attribute (profilers that replay
  *              kernels cannot launch a cooperative cluster kernel).  Its CTAs
@@ -163,6 +169,7 @@ typedef struct moe_config {
   int32_t test_unfilled_minibatch;
   int32_t clc;
   int32_t plain_launch;
+  int32_t pad_odd_tiles;
 } moe_config;
 
 /*

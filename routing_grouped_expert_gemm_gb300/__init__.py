@@ -55,7 +55,7 @@ class moe_config(ctypes.Structure):
                 ("timeout_ms", ctypes.c_int32), ("dispatch", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32),
                 ("mma_pair", ctypes.c_int32), ("raster", ctypes.c_int32),
                 ("test_unfilled_minibatch", ctypes.c_int32), ("clc", ctypes.c_int32),
-                ("plain_launch", ctypes.c_int32)]
+                ("plain_launch", ctypes.c_int32), ("pad_odd_tiles", ctypes.c_int32)]
 
 
 class moe_weights(ctypes.Structure):
@@ -191,7 +191,8 @@ class Plan:
 
 def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precision=MOE_PREC_BF16, minibatch=0,
                     ring_slots=0, gather_ctas=0, gemm_ctas=0, lag=1, timeout_ms=0, dispatch=MOE_DISPATCH_RING,
-                    l2_prefetch=0, mma_pair=0, raster=0, test_unfilled_minibatch=0, clc=0, plain_launch=0) -> Plan:
+                    l2_prefetch=0, mma_pair=0, raster=0, test_unfilled_minibatch=0, clc=0, plain_launch=0,
+                    pad_odd_tiles=0) -> Plan:
     if isinstance(score_fn, str):
         score_fn = {"sigmoid": MOE_SCORE_SIGMOID, "softmax": MOE_SCORE_SOFTMAX}[score_fn]
     if isinstance(precision, str):
@@ -199,7 +200,8 @@ def moe_plan_create(T_max, D, I, E, k, I_s=0, score_fn=MOE_SCORE_SIGMOID, precis
     if isinstance(dispatch, str):
         dispatch = {"ring": MOE_DISPATCH_RING, "direct": MOE_DISPATCH_DIRECT, "spread": MOE_DISPATCH_SPREAD}[dispatch]
     cfg = moe_config(T_max, D, I, E, k, I_s, score_fn, precision, minibatch, ring_slots, gather_ctas, gemm_ctas,
-                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster, test_unfilled_minibatch, clc, plain_launch)
+                     lag, timeout_ms, dispatch, l2_prefetch, mma_pair, raster, test_unfilled_minibatch, clc, plain_launch,
+                     pad_odd_tiles)
     h = ctypes.c_void_p()
     rc = lib().moe_plan_create(ctypes.byref(cfg), ctypes.byref(h))
     if rc != MOE_OK:

@@ -191,6 +191,7 @@ int moe_plan_create(const moe_config* cfg_in, moe_plan** out) {
   // cluster launch control schedules the one-CTA kernel
   if (c.clc != 0 && c.clc != 1) return MOE_ERR_INVALID_ARG;
   if (c.plain_launch != 0 && c.plain_launch != 1) return MOE_ERR_INVALID_ARG;
+  if (c.pad_odd_tiles != 0 && c.pad_odd_tiles != 1) return MOE_ERR_INVALID_ARG;
   if (c.clc && c.mma_pair) return MOE_ERR_INVALID_ARG;
 #ifdef MOE_DEBUG_LOG
   if (c.clc) return MOE_ERR_INVALID_ARG;  // the progress records are sized for the persistent grid
@@ -367,6 +368,7 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
   p.test_unfilled = c.test_unfilled_minibatch;
   p.clc = c.clc;
   p.plain_launch = c.plain_launch;
+  p.half_tiles = c.mma_pair && c.precision == MOE_PREC_BF16 && !c.pad_odd_tiles ? 1 : 0;
   p.x = static_cast<const bf16*>(x);
   p.b_router = w->b_router;
   p.status = reinterpret_cast<int*>(ws + L.status);
@@ -443,6 +445,10 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
     rc |= encode_bf16_2d(pl, &tm.w_gate, w->W_gate, c.E * c.I, c.D, BN_UP);
     rc |= encode_bf16_2d(pl, &tm.ring_h, p.ring_h, ring_rows, c.I, BM);
     rc |= encode_bf16_2d(pl, &tm.w_down, w->W_down, c.E * c.D, c.I, down_box);
+    if (p.half_tiles) {  // a split M-tile's 64 rows per CTA
+      rc |= encode_bf16_2d(pl, &tm.ring_x64, p.ring_x, ring_rows, c.D, BM / 2);
+      rc |= encode_bf16_2d(pl, &tm.ring_h64, p.ring_h, ring_rows, c.I, BM / 2);
+    }
   }
   if (shared) {
     rc |= encode_bf16_2d(pl, &tm.ws_up, w->Ws_up, c.I_s, c.D, BN_UP);

@@ -78,7 +78,8 @@ struct __align__(16) Task {  // 64 bytes
   int dep1, need1;
   int done0, done1;  // counters incremented when the tile is stored (-1: none)
   int mt;            // global M-tile index (routed) / token tile (shared)
-  int pad[2];
+  int half;          // 1: one 64-row half of a routed M-tile that the pair runs as one M = 128 MMA
+  int pad;
 };
 static_assert(sizeof(Task) == 64, "task record is 64 bytes");
 
@@ -95,6 +96,7 @@ struct FwdParams {
   int direct;           // 1: GEMM producers gather A rows from x themselves (no gather CTAs, no x ring)
   int pair;             // 1: GEMM CTAs run as pairs, tasks 2i and 2i + 1 share one cta_group::2 MMA
   int plain_launch;     // 1: the persistent kernel is launched without the cooperative attribute (profiling)
+  int half_tiles;       // 1: a segment's odd last M-tile is split over the pair (BF16 CTA pairs)
   int spread;           // 1: two spare warps of every GEMM CTA fill the ring (no gather CTAs)
   int gparts;           // parts the ring fill of a minibatch is split into (gather CTAs or GEMM CTAs)
   int raster;           // M-tiles per group of a segment's up/gate tiles (column tiles swept per group)
@@ -247,6 +249,8 @@ struct TensorMaps {
   CUtensorMap w_up;     // [E*I, D]          box {64, 128}
   CUtensorMap w_gate;   // [E*I, D]          box {64, 128}
   CUtensorMap ring_h;   // [slots*b, I]      box {64, 128}
+  CUtensorMap ring_x64; // BF16 pairs, split M-tiles: [slots*b, D] box {64, 64}
+  CUtensorMap ring_h64; // ... [slots*b, I] box {64, 64}
   CUtensorMap w_down;   // [E*D, I]          box {64, 256}
   CUtensorMap ws_up;    // [I_s, D]          box {64, 128}
   CUtensorMap ws_gate;  // [I_s, D]          box {64, 128}

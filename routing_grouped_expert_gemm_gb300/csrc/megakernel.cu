@@ -308,6 +308,7 @@ __device__ void gather_role(const FwdParams& p, volatile int* s_flag, uint8_t* b
 // ------------------------------------------------------------------ operand selection
 struct Operands {
   const CUtensorMap* a;
+  const CUtensorMap* a64;  // routed BF16 pair tiles split over the pair: 64-row A boxes
   const CUtensorMap* b0;
   const CUtensorMap* b1;  // null: one 256-row B box
   int b_row;
@@ -323,19 +324,19 @@ __device__ __forceinline__ Operands task_operands(const TensorMaps& maps, const 
   const int kstep = p.mx ? BK_MX : BK;  // routed tensor maps are E4M3 (MXFP8) or bf16
   switch (t.kind) {
     case TASK_R1:
-      o.a = &maps.ring_x; o.b0 = &maps.w_up; o.b1 = &maps.w_gate;
+      o.a = &maps.ring_x; o.a64 = &maps.ring_x64; o.b0 = &maps.w_up; o.b1 = &maps.w_gate;
       o.b_row = t.e * p.I + t.n * BN_UP; o.nk = p.D / kstep;
       break;
     case TASK_R2:
-      o.a = &maps.ring_h; o.b0 = &maps.w_down; o.b1 = nullptr;
+      o.a = &maps.ring_h; o.a64 = &maps.ring_h64; o.b0 = &maps.w_down; o.b1 = nullptr;
       o.b_row = t.e * p.D + t.n * BN_DOWN; o.nk = p.I / kstep;
       break;
     case TASK_S1:
-      o.a = &maps.x; o.b0 = &maps.ws_up; o.b1 = &maps.ws_gate;
+      o.a = &maps.x; o.a64 = nullptr; o.b0 = &maps.ws_up; o.b1 = &maps.ws_gate;
       o.b_row = t.n * BN_UP; o.nk = p.D / BK;
       break;
     default:  // TASK_S2
-      o.a = &maps.h_s; o.b0 = &maps.ws_down; o.b1 = nullptr;
+      o.a = &maps.h_s; o.a64 = nullptr; o.b0 = &maps.ws_down; o.b1 = nullptr;
       o.b_row = t.n * BN_DOWN; o.nk = p.I_s / BK;
       break;
   }
@@ -456,6 +457,46 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
   }
 }
 
+// Up/gate tile split over a pair (one M = 128 MMA): the CTA's 64 rows hold
+// their up columns in TMEM lanes 0-63 and their gate columns in lanes 64-127,
+// both at columns 0-127.  The warp of lanes 64 + 32 q' stages each 32-column
+// chunk of gate values in its staging block; the warp of lanes 32 q' (same
+// rows) reads them after a named barrier of the two warps, forms h and stores
+// it.  A second barrier frees the block for the next chunk.
+__device__ void epilogue_swiglu_split(uint32_t taddr, EpiStage& st_own, const EpiStage& st_gate, bf16* dst,
+                                      size_t ld, int nrows, const AccRelease& rel, bool gate_warp, int bar_id) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int c = 0; c < BN_UP; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+    tmem_ld_wait();
+    if (c == 0) release_head(rel);
+    if (c + 32 == BN_UP) release_acc(rel);
+    if (gate_warp) {
+      float g[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(r[j]);
+      stage_block(st_own, g);
+      named_bar_sync(bar_id, 64);  // the chunk's gate values are staged
+      named_bar_sync(bar_id, 64);  // ... and read
+    } else {
+      named_bar_sync(bar_id, 64);
+      float h[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) h[j] = silu_f32(st_gate.v[lane][j]) * __uint_as_float(r[j]);
+      named_bar_sync(bar_id, 64);
+      stage_block(st_own, h);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
+        if (rr < nrows) *reinterpret_cast<uint2*>(dst + (size_t)rr * ld + c + cc) = pack_bf16x4(staged4(st_own, rr, cc));
+      }
+      __syncwarp();
+    }
+  }
+}
+
 // MXFP8 up/gate tile -> h quantised per 32 columns: E4M3 codes into the h ring
 // (thread = row, 128 bytes) and one 32-bit word of four E8M0 codes into the
 // tile's scale block (this tile's 128 columns are one 128-wide K step of the
@@ -497,17 +538,20 @@ __device__ void epilogue_swiglu_mx(uint32_t taddr, uint8_t* dst_row, uint8_t* sf
 // read (with two accumulator buffers the MMA issuer rarely waits for it).
 // A value outside the fp16 range (or NaN) is saturated and raises
 // FLAG_STAGING_OVERFLOW in flags (the forward goes on; its status says so).
+// ncols of the warp's 32 TMEM lanes (from taddr) are output columns col0 .. col0 + ncols - 1 of
+// its rows: all 256 columns, or (a split tile: lanes 0-63 columns 0-127, lanes 64-127 columns
+// 128-255 of the same 64 rows) 128 of them
 __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y, long long y_mine, int nrows,
-                                         const AccRelease& rel, int* flags) {
+                                         const AccRelease& rel, int* flags, int ncols = BN_DOWN, int col0 = 0) {
   const int lane = threadIdx.x & 31;
   bool ovf = false;
 #pragma unroll 1
-  for (int c = 0; c < BN_DOWN; c += 32) {
+  for (int c = 0; c < ncols; c += 32) {
     uint32_t r[32];
     tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
     tmem_ld_wait();
     if (c == 0) release_head(rel);
-    if (c + 32 == BN_DOWN) release_acc(rel);
+    if (c + 32 == ncols) release_acc(rel);
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -520,7 +564,8 @@ __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y
         const float4 f = staged4(st, rr, cc);
         const float a = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
         ovf |= !(a <= 65504.0f) || f.x != f.x || f.y != f.y || f.z != f.z || f.w != f.w;
-        *reinterpret_cast<uint2*>(Y + yr + c + cc) = make_uint2(pack_f16x2_sat(f.x, f.y), pack_f16x2_sat(f.z, f.w));
+        *reinterpret_cast<uint2*>(Y + yr + col0 + c + cc) =
+            make_uint2(pack_f16x2_sat(f.x, f.y), pack_f16x2_sat(f.z, f.w));
       }
     }
     __syncwarp();
@@ -942,10 +987,14 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           uint8_t* sa = smem + stage * G::stride;
           uint8_t* sb = sa + A_STAGE_BYTES;
           const int kc = kb * (mx ? BK_MX : BK);
+          // a split tile: 64 A rows per CTA (8 KB)
+          const bool half = !kMxPair && t.half;
           if (leader)
-            mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(mx ? PAIR_MX_STAGE_TX : PAIR_STAGE_BYTES));
+            mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(mx ? PAIR_MX_STAGE_TX
+                                                                   : (half ? PAIR_STAGE_BYTES - A_STAGE_BYTES / 2
+                                                                           : PAIR_STAGE_BYTES)));
           const uint32_t fb = full_even + stage * 8u;
-          tma_load_2d_pair(sa, o.a, fb, kc, t.a_row);
+          tma_load_2d_pair(sa, half ? o.a64 : o.a, fb, kc, t.a_row);
           tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
           if constexpr (kMxPair) {
             if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
@@ -1103,6 +1152,8 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
           const int kind = p.tasks[walk.task(u)].kind;
           const bool mx = task_is_mx(p, kind);
           const int nk = task_nk(p, kind);
+          // a split tile (BF16 pairs): one M = 128 MMA, 64 rows per CTA
+          const uint32_t idesc_u = (kPair && !kMxPair && p.tasks[walk.task(u)].half) ? idesc_bf16_f32(BM, 256) : idesc;
           const uint32_t acc = accs.next();
           DBG_SET(p, DBG_MMA_UNIT, u);
           DBG_SET(p, DBG_MMA_ACC, acc);
@@ -1165,7 +1216,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
               } else {
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                  mma_bf16_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc,
+                  mma_bf16_pair(d, sdesc_kmajor_sw128(a_addr + kk * 32), sdesc_kmajor_sw128(b_addr + kk * 32), idesc_u,
                                 (kb | kk) != 0 ? 1u : 0u);
               }
               mma_commit_pair(&empty[stage], 0x3);
@@ -1271,7 +1322,20 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 #endif
         EpiStage& st = epi[q];
         const AccRelease rel{&tempty[acc], tempty_even + acc * 8u, &thead[acc], thead_even + acc * 8u, kPair};
-        if (t.kind == TASK_R1 && p.mx) {
+        const bool split = kPair && !kMxPair && t.half;  // a routed tile split over the pair
+        if (split && t.kind == TASK_R1) {
+          // lanes 32 (q % 2) + lane of the CTA's 64 rows; gate values in the warp of quadrant q % 2 + 2
+          const int hq = q & 1;
+          epilogue_swiglu_split(taddr, st, epi[hq + 2],
+                                p.ring_h + (size_t)(t.out_row + 32 * hq) * p.I + t.n * BN_UP, p.I,
+                                min(32, max(0, t.rows - 32 * hq)), rel, q >= 2, 3 + hq);
+        } else if (split) {  // TASK_R2: lanes 0-63 output columns 0-127, lanes 64-127 columns 128-255
+          const int hq = q & 1, hrow = 32 * hq + lane;
+          const int j = hrow < t.rows ? p.sched[(size_t)(t.p0 + hrow) * 3 + 2] : 0;
+          epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n),
+                                   min(32, max(0, t.rows - 32 * hq)), rel, p.status + 1, BN_DOWN / 2,
+                                   (q >> 1) * (BN_DOWN / 2));
+        } else if (t.kind == TASK_R1 && p.mx) {
           epilogue_swiglu_mx(taddr, reinterpret_cast<uint8_t*>(p.ring_h) + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
                              p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows, rel);
         } else if (t.kind == TASK_R1) {

@@ -268,8 +268,11 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
   // per-minibatch task counts and the first task of every step
   if (blockIdx.x == 0) {
     for (int m = tid; m < n_mb; m += blockDim.x) {
-      p.meta[META_MB + 4 * m] = fits ? mb_tiles[m] * p.N1 : 0;
-      p.meta[META_MB + 4 * m + 1] = fits ? mb_tiles[m] * p.N2 : 0;
+      // tasks that complete per column tile: one per M-tile, and with split tail
+      // tiles one per pair slot (both halves of a split tile complete)
+      const int inc = p.half_tiles ? mb_ptiles[m] : mb_tiles[m];
+      p.meta[META_MB + 4 * m] = fits ? inc * p.N1 : 0;
+      p.meta[META_MB + 4 * m + 1] = fits ? inc * p.N2 : 0;
       p.meta[META_MB + 4 * m + 2] = fits ? mt_first[m] : 0;
       p.meta[META_MB + 4 * m + 3] = fits ? mb_tiles[m] : 0;
     }
@@ -291,7 +294,7 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
       p.meta[META_N_TASKS] = ok ? (int)total : 0;
       p.meta[META_N_MTILES] = nmt_tot;
       int y = 0;
-      for (int m = 0; m < n_mb; ++m) y += mb_tiles[m] * p.N2;
+      for (int m = 0; m < n_mb; ++m) y += (p.half_tiles ? mb_ptiles[m] : mb_tiles[m]) * p.N2;
       y += p.n_smtiles * p.N2s;
       p.meta[META_TOTAL_Y] = ok ? y : 0;
     }
@@ -325,7 +328,8 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
     tk.done0 = !down && real ? ctr_shready(p, mt) : -1;
     tk.done1 = down && real ? ctr_ydone() : -1;  // the shared output is staging slot k
     tk.mt = mtr;
-    tk.pad[0] = tk.pad[1] = 0;
+    tk.half = 0;
+    tk.pad = 0;
     store_task(p.tasks + (down ? (int)total - n_s2 + qq : qq), tk);
   }
   // routed tasks: CTA c fills experts c, c + gridDim.x, ...; its threads stride
@@ -344,7 +348,10 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
       const int sr2 = m + p.lag;
       const int r2_base =
           n_s1 + step_off[sr2] + (sr2 < n_mb ? mb_ptiles[sr2] * p.N1 : 0) + p.N2 * (ptb - mtp_first[m]);
-      const int need_h = m >= p.slots ? mb_tiles[m - p.slots] * p.N2 : 0;
+      const int need_h = m >= p.slots ? (p.half_tiles ? mb_ptiles[m - p.slots] : mb_tiles[m - p.slots]) * p.N2 : 0;
+      // BF16 pairs: an odd segment's last M-tile is split over the pair's two
+      // tasks (rows 0-63 and 64-127, one M = 128 MMA) instead of padded
+      const bool split_tail = p.half_tiles && (cnt & 1);
       for (int q = tid; q < cntp * (p.N1 + p.N2); q += blockDim.x) {
         const bool down = q >= cntp * p.N1;
         const int qq = down ? q - cntp * p.N1 : q;
@@ -358,17 +365,20 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           i = grp * p.raster + within % gc;
           n = within / gc;
         }
-        const bool real = i < cnt;
-        const int ir = real ? i : i - 1;  // an empty partner takes its partner's rows (A: none)
-        const int r0 = a + ir * BM;
+        const bool half = split_tail && i >= cnt - 1;  // half h = i - (cnt - 1) of the last tile
+        const bool real = i < cnt || half;
+        const int ir = half ? cnt - 1 : (real ? i : i - 1);  // an empty partner takes its partner's rows (A: none)
+        const int hh = half ? i - (cnt - 1) : 0;
+        const int r0 = a + ir * BM + (BM / 2) * hh;
         Task tk;
         tk.kind = down ? TASK_R2 : TASK_R1;
         tk.n = n;
         tk.e = e;
         tk.out_row = slot_row + (r0 - m * b);
         tk.a_row = real ? tk.out_row : NO_ROWS;
-        tk.rows = real ? min(BM, z - r0) : 0;
+        tk.rows = half ? max(0, min(BM / 2, z - r0)) : (real ? min(BM, z - r0) : 0);
         tk.p0 = r0;
+        tk.half = half ? 1 : 0;
         if (!real) {
           tk.dep0 = tk.dep1 = tk.done0 = tk.done1 = -1;
           tk.need0 = tk.need1 = 0;
@@ -377,18 +387,18 @@ __device__ void build_tasks(const FwdParams& p, const int* sS, int* dsm) {
           tk.need0 = p.gparts;
           tk.dep1 = m >= p.slots ? ctr_r2(p, m - p.slots) : -1;
           tk.need1 = need_h;
-          tk.done0 = ctr_hready(p, mtb + i);
+          tk.done0 = ctr_hready(p, mtb + ir);
           tk.done1 = ctr_r1(p, m);
         } else {
-          tk.dep0 = ctr_hready(p, mtb + i);
-          tk.need0 = p.N1;
+          tk.dep0 = ctr_hready(p, mtb + ir);
+          tk.need0 = half ? 2 * p.N1 : p.N1;  // both halves of a split tile count on its counter
           tk.dep1 = -1;
           tk.need1 = 0;
           tk.done0 = ctr_r2(p, m);
           tk.done1 = ctr_ydone();
         }
         tk.mt = mtb + ir;
-        tk.pad[0] = tk.pad[1] = 0;
+        tk.pad = 0;
         store_task(p.tasks + (down ? r2_base : r1_base) + qq, tk);
       }
       for (int i = tid; i < cnt; i += blockDim.x) {  // the M-tile table (the gather walks it)

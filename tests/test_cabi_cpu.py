@@ -100,7 +100,8 @@ def test_plan_rejects_bad_knobs(L):
                dict(mma_pair=1, precision="mxfp8", dispatch="direct"), dict(mma_pair=2), dict(raster=-1),
                dict(l2_prefetch=65), dict(dispatch=7), dict(gemm_ctas=-1),
                dict(test_unfilled_minibatch=-1), dict(test_unfilled_minibatch=1, dispatch="direct"),
-               dict(clc=2), dict(clc=1, mma_pair=1), dict(plain_launch=2), dict(plain_launch=-1)):
+               dict(clc=2), dict(clc=1, mma_pair=1), dict(plain_launch=2), dict(plain_launch=-1),
+               dict(pad_odd_tiles=2), dict(pad_odd_tiles=-1, mma_pair=1)):
         with pytest.raises(rg.MoEError) as ei:
             rg.moe_plan_create(**base, **kw)
         assert ei.value.code == rg.MOE_ERR_INVALID_ARG, kw
@@ -114,7 +115,7 @@ def test_valid_knobs_pass_validation(L):
                dict(mma_pair=1, gather_ctas=3, dispatch="spread"), dict(dispatch="direct", precision="mxfp8"),
                dict(raster=3, mma_pair=1), dict(k=16, E=512, I_s=0), dict(test_unfilled_minibatch=1),
                dict(test_unfilled_minibatch=2, dispatch="spread"), dict(clc=1), dict(clc=1, dispatch="spread"),
-               dict(plain_launch=1), dict(plain_launch=1, mma_pair=1)):
+               dict(plain_launch=1), dict(plain_launch=1, mma_pair=1), dict(pad_odd_tiles=1, mma_pair=1)):
         with pytest.raises(rg.MoEError) as ei:
             rg.moe_plan_create(**{**base, **kw})
         assert ei.value.code in (rg.MOE_ERR_CUDA, rg.MOE_ERR_UNSUPPORTED_DEVICE), kw

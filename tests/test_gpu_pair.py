@@ -4,9 +4,11 @@ weight tile) against the fp64 oracle, with the same bars as the one-CTA
 kernel: routing and schedule bit-exact, outputs within rel-L2 1e-2 and
 max-abs 3e-2 rms, repeated runs and scheduling knobs bitwise identical.
 
-The cases cover segments with an odd number of M-tiles (the pair's second
-task is an empty partner), a single token, a ragged token tail, no shared
-expert, one expert taking every token and the full-size DSV3 workload."""
+The cases cover segments with an odd number of M-tiles (with bf16 the last
+tile is split over the pair, 64 rows per CTA in one M = 128 MMA; with MXFP8,
+or pad_odd_tiles = 1, the pair's second task is an empty partner), a single
+token, a ragged token tail, no shared expert, one expert taking every token
+and the full-size DSV3 workload."""
 import numpy as np
 import pytest
 import torch
@@ -90,6 +92,31 @@ def test_pair_plain_launch_is_bitwise_identical(precision):
         assert res["status"] == 0
         outs.append(res["out"].view(torch.int16).cpu().numpy())
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_pair_padded_odd_tiles_against_oracle():
+    # the empty-partner form of an odd segment's last M-tile (bf16)
+    run_and_check(small(1000, 512, 256, 32, 6, 256, cid=315), minibatch=1024, ring_slots=3, gather_ctas=4,
+                  mma_pair=1, pad_odd_tiles=1)
+
+
+@pytest.mark.parametrize("T", [1, 64, 65, 300])
+def test_pair_split_tail_tiles_bitwise_equal_to_padded(T):
+    """Splitting an odd segment's last M-tile over the pair (64 rows per CTA,
+    one M = 128 MMA) gives the bits of the padded form (one M = 256 MMA with an
+    empty partner); T = 64 / 65 put a tile edge at the split."""
+    import gpu_util as g
+    inp = small(1000, 512, 256, 32, 6, 256, cid=316)
+    x = g.to_dev_bf16(inp.x[:T])
+    for kw in (dict(minibatch=512, ring_slots=3, dispatch="spread"),
+               dict(minibatch=256, ring_slots=2, gather_ctas=2, raster=2)):
+        outs = []
+        for pad in (1, 0):
+            layer = g.Layer(inp, T_max=inp.T, mma_pair=1, pad_odd_tiles=pad, **kw)
+            res = layer.run(x, T, poison=True)
+            assert res["status"] == 0
+            outs.append(res["out"].view(torch.int16).cpu().numpy())
+        assert np.array_equal(outs[0], outs[1]), f"output bits differ for {kw}"
 
 
 def test_pair_rejects_unsupported_modes():
