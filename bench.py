@@ -269,13 +269,19 @@ def l2_note(shape) -> str:
 
 
 # ----------------------------------------------------------------------------- recorded DRAM traffic
+# the sources that decide what the persistent kernel launch does: its code, the task
+# schedule, the plan and launch set-up, the MXFP8 layouts and the C header (the router,
+# the backward pass and the layout probes are separate launches)
+TRAFFIC_SOURCES = ("api.cu", "common.cuh", "megakernel.cu", "mxfp8.cu", "plan.cuh", "ptx.cuh", "schedule.cu")
+
+
 def kernel_sources_hash() -> str:
-    """sha256 over the CUDA sources and the C header: a recorded ncu traffic figure
-    applies only to the kernels it was taken from."""
+    """sha256 over the persistent kernel's sources and the C header: a recorded ncu
+    traffic figure applies only to the kernel it was taken from."""
     import hashlib
     root = os.path.dirname(os.path.abspath(__file__))
     csrc = os.path.join(root, "routing_grouped_expert_gemm_gb300", "csrc")
-    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh")))
+    files = [os.path.join(csrc, f) for f in TRAFFIC_SOURCES]
     files.append(os.path.join(root, "include", "moe.h"))
     h = hashlib.sha256()
     for f in files:
