@@ -108,6 +108,13 @@ def test_k_equals_E_and_top1():
     run_and_check(small(300, 256, 128, 8, 1, 0, cid=306), minibatch=128, ring_slots=2)
 
 
+@pytest.mark.parametrize("mma_pair", [0, 1])
+def test_largest_top_k_with_shared_expert(mma_pair):
+    # k = 16 (the largest supported) plus the shared expert: 17 staging slots per token
+    run_and_check(small(600, 512, 256, 64, 16, 256, cid=309), minibatch=2048, ring_slots=2, dispatch="spread",
+                  mma_pair=mma_pair)
+
+
 def test_bitwise_deterministic_across_knobs():
     """Repeated runs and every scheduling knob give the same bits (each output
     row is computed by one tile with a fixed K order, the combine runs in a
