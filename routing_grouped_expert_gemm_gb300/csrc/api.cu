@@ -448,6 +448,8 @@ int moe_fwd(const moe_plan* pl, int64_t T, const void* x, const moe_weights* w, 
     if (p.half_tiles) {  // a split M-tile's 64 rows per CTA
       rc |= encode_bf16_2d(pl, &tm.ring_x64, p.ring_x, ring_rows, c.D, BM / 2);
       rc |= encode_bf16_2d(pl, &tm.ring_h64, p.ring_h, ring_rows, c.I, BM / 2);
+      rc |= encode_bf16_2d(pl, &tm.w_up64, w->W_up, c.E * c.I, c.D, BM / 2);
+      rc |= encode_bf16_2d(pl, &tm.w_gate64, w->W_gate, c.E * c.I, c.D, BM / 2);
     }
   }
   if (shared) {

@@ -36,7 +36,7 @@ static_assert(STAGE_BYTES + SF_STAGE_BYTES <= STAGE_STRIDE && STAGE_STRIDE % 102
 // 256 B rows (up or gate for GEMM1, one half of the output columns for GEMM2)
 constexpr int PAIR_B_STAGE_BYTES = 128 * BK * 2;  // 16 KB
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + PAIR_B_STAGE_BYTES;  // 32 KB per CTA
-constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_STAGES = 7;  // BF16 pairs: the epilogue stores rows from registers, no staging blocks
 // CTA pairs, MXFP8 routed tiles: per CTA and stage its A codes and its half
 // of B's codes in the 32 KB stage, and in a separate array of 1.5 KB slots
 // (one per stage, after the stages) the A scale block of its rows and B's two
@@ -251,6 +251,8 @@ struct TensorMaps {
   CUtensorMap ring_h;   // [slots*b, I]      box {64, 128}
   CUtensorMap ring_x64; // BF16 pairs, split M-tiles: [slots*b, D] box {64, 64}
   CUtensorMap ring_h64; // ... [slots*b, I] box {64, 64}
+  CUtensorMap w_up64;   // ... [E*I, D] box {64, 64}: 64 up rows and
+  CUtensorMap w_gate64; //     64 gate rows per CTA
   CUtensorMap w_down;   // [E*D, I]          box {64, 256}
   CUtensorMap ws_up;    // [I_s, D]          box {64, 128}
   CUtensorMap ws_gate;  // [I_s, D]          box {64, 128}

@@ -457,46 +457,6 @@ __device__ void epilogue_swiglu(uint32_t taddr, EpiStage& st, bf16* dst, size_t 
   }
 }
 
-// Up/gate tile split over a pair (one M = 128 MMA): the CTA's 64 rows hold
-// their up columns in TMEM lanes 0-63 and their gate columns in lanes 64-127,
-// both at columns 0-127.  The warp of lanes 64 + 32 q' stages each 32-column
-// chunk of gate values in its staging block; the warp of lanes 32 q' (same
-// rows) reads them after a named barrier of the two warps, forms h and stores
-// it.  A second barrier frees the block for the next chunk.
-__device__ void epilogue_swiglu_split(uint32_t taddr, EpiStage& st_own, const EpiStage& st_gate, bf16* dst,
-                                      size_t ld, int nrows, const AccRelease& rel, bool gate_warp, int bar_id) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int c = 0; c < BN_UP; c += 32) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
-    tmem_ld_wait();
-    if (c == 0) release_head(rel);
-    if (c + 32 == BN_UP) release_acc(rel);
-    if (gate_warp) {
-      float g[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(r[j]);
-      stage_block(st_own, g);
-      named_bar_sync(bar_id, 64);  // the chunk's gate values are staged
-      named_bar_sync(bar_id, 64);  // ... and read
-    } else {
-      named_bar_sync(bar_id, 64);
-      float h[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) h[j] = silu_f32(st_gate.v[lane][j]) * __uint_as_float(r[j]);
-      named_bar_sync(bar_id, 64);
-      stage_block(st_own, h);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = 4 * i + (lane >> 3), cc = 4 * (lane & 7);
-        if (rr < nrows) *reinterpret_cast<uint2*>(dst + (size_t)rr * ld + c + cc) = pack_bf16x4(staged4(st_own, rr, cc));
-      }
-      __syncwarp();
-    }
-  }
-}
-
 // MXFP8 up/gate tile -> h quantised per 32 columns: E4M3 codes into the h ring
 // (thread = row, 128 bytes) and one 32-bit word of four E8M0 codes into the
 // tile's scale block (this tile's 128 columns are one 128-wide K step of the
@@ -571,6 +531,65 @@ __device__ void epilogue_copy_f16_staged(uint32_t taddr, EpiStage& st, __half* Y
     __syncwarp();
   }
   if (__any_sync(0xffffffffu, ovf) && lane == 0) atomicOr(flags, FLAG_STAGING_OVERFLOW);
+}
+
+// BF16 CTA pairs store their epilogue rows from registers: lane l holds 32
+// columns of its row per TMEM load and writes them as two 32-byte vectors
+// (full L2 sectors), so the kernel keeps no staging blocks and has room for a
+// seventh operand stage.  live: the row is a real tile row.
+//
+// Up/gate tile -> h = SiLU(gate) * up (bf16): up columns at taddr + c, gate
+// columns at taddr + gate_off + c, c < ncols (a whole tile: 128 and 128; a tile
+// split over the pair: this lane's 64 h columns, up then gate); dst: the row's
+// first h column.
+__device__ void epilogue_swiglu_direct(uint32_t taddr, bf16* dst, bool live, const AccRelease& rel, int gate_off,
+                                       int ncols) {
+#pragma unroll 1
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t u[32], g[32];
+    tmem_ld_32x32b_x32(taddr + (uint32_t)c, u);
+    tmem_ld_32x32b_x32(taddr + (uint32_t)(gate_off + c), g);
+    tmem_ld_wait();
+    if (c == 0) release_head(rel);
+    if (c + 32 == ncols) release_acc(rel);  // last TMEM read of this tile
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      w[j] = pack_bf16x2(silu_f32(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]),
+                         silu_f32(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+    if (live) {
+      st_global_v8(dst + c, w);
+      st_global_v8(dst + c + 16, w + 8);
+    }
+  }
+}
+
+// Down-projection tile -> fp16 staging row: ncols TMEM columns from taddr are
+// output columns 0 .. ncols - 1 from yrow (all 256, or 128 for a split tile);
+// saturation at the fp16 maximum and NaN are flagged as in the staged form.
+__device__ void epilogue_copy_f16_direct(uint32_t taddr, __half* yrow, bool live, const AccRelease& rel, int* flags,
+                                         int ncols) {
+  bool ovf = false;
+#pragma unroll 1
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+    tmem_ld_wait();
+    if (c == 0) release_head(rel);
+    if (c + 32 == ncols) release_acc(rel);
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+      ovf |= !(fmaxf(fabsf(a), fabsf(b)) <= 65504.0f) || a != a || b != b;
+      w[j] = pack_f16x2_sat(a, b);
+    }
+    if (live) {
+      st_global_v8(yrow + c, w);
+      st_global_v8(yrow + c + 16, w + 8);
+    }
+  }
+  if (__any_sync(0xffffffffu, ovf && live) && (threadIdx.x & 31) == 0) atomicOr(flags, FLAG_STAGING_OVERFLOW);
 }
 
 // ------------------------------------------------------------------ combine
@@ -715,16 +734,28 @@ __device__ void combine_role(const FwdParams& p, uint8_t* buf, int buf_bytes, ui
 // variables (BAR_BYTES) and the epilogue staging.
 constexpr int BAR_BYTES = 512;
 constexpr int QN = 8;  // unit queue slots (the producer runs at most a few units ahead)
+// kDirectEpi (BF16 pairs): the epilogue stores rows straight from registers,
+// so the area after the barriers only holds the combine's and the gather's
+// barriers (1.5 KB) and the stages take a seventh slot.
 template <bool kPair, bool kMx = false>
 struct MegaGeom {
+  static constexpr bool kDirectEpi = kPair && !kMx;
   static constexpr int stages = kPair ? (kMx ? PAIR_MX_STAGES : PAIR_STAGES) : STAGES;
   static constexpr int stride = kPair ? PAIR_STAGE_BYTES : STAGE_STRIDE;
   static constexpr int sf_bytes = kMx ? stages * SF_STAGE_BYTES : 0;
-  static constexpr int smem_bytes = stages * stride + sf_bytes + 1024 /*align*/ + BAR_BYTES + EPI_STAGE_BYTES;
+  static constexpr int epi_bytes = kDirectEpi ? 1536 : EPI_STAGE_BYTES;
+  static constexpr int smem_bytes = stages * stride + sf_bytes + 1024 /*align*/ + BAR_BYTES + epi_bytes;
 };
 static_assert(MegaGeom<true>::smem_bytes <= 232448 && MegaGeom<false>::smem_bytes <= 232448 &&
                   MegaGeom<true, true>::smem_bytes <= 232448,
               "shared memory");
+// the small area (BF16 pairs) holds the gather's barriers and, past them, the
+// combine's barriers and claim word; the gather's token table goes to the
+// stage buffers there, which keep room for at least 12 rows of D <= 8192
+static_assert(CMB_BAR_OFFSET + (CMB_BUFS + 1) * 8 <= MegaGeom<true>::epi_bytes && GATHER_BUFS * 8 <= CMB_BAR_OFFSET &&
+                  EPI_STAGE_BYTES >= GATHER_BUFS * 8 + GATHER_TOK_CHUNK * 4 &&
+                  MegaGeom<true>::stages * PAIR_STAGE_BYTES - GATHER_TOK_CHUNK * 4 >= 12 * 8192 * 2,
+              "shared areas of the gather and the combine");
 
 template <bool kPair>
 __device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
@@ -779,7 +810,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
   uint8_t* smem = align_1024_mk(smem_raw);
   uint8_t* sf_slots = smem + NST * G::stride;  // pairs with MXFP8 tiles: scale blocks per stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf_slots + G::sf_bytes);
-  static_assert(2 * 6 + 7 <= 24 && 48 * 8 + QN * 4 <= 52 * 8 && 56 * 8 <= BAR_BYTES, "barrier area");
+  static_assert(2 * NST + 7 <= 24 && 48 * 8 + QN * 4 <= 52 * 8 && 56 * 8 <= BAR_BYTES, "barrier area");
   uint64_t* full = bars;
   uint64_t* empty = bars + NST;
   uint64_t* tfull = bars + 2 * NST;
@@ -816,8 +847,16 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
 
   if (is_gather) {
     // the stage buffers hold rows in flight; the barriers live in the (unused) epilogue staging area
-    gather_role(p, s_flag, smem, NST * G::stride, reinterpret_cast<uint64_t*>(epi),
-                reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(epi) + GATHER_BUFS));
+    if constexpr (G::kDirectEpi) {
+      // the small area after the barriers holds the gather's barriers only; its token
+      // table (GATHER_TOK_CHUNK ints) takes the end of the stage buffers
+      constexpr int rows_bytes = NST * G::stride - GATHER_TOK_CHUNK * 4;
+      gather_role(p, s_flag, smem, rows_bytes, reinterpret_cast<uint64_t*>(epi),
+                  reinterpret_cast<int*>(smem + rows_bytes));
+    } else {
+      gather_role(p, s_flag, smem, NST * G::stride, reinterpret_cast<uint64_t*>(epi),
+                  reinterpret_cast<int*>(reinterpret_cast<uint64_t*>(epi) + GATHER_BUFS));
+    }
     __syncthreads();
   } else {
     const int cta = blockIdx.x - p.G;
@@ -995,7 +1034,15 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
                                                                            : PAIR_STAGE_BYTES)));
           const uint32_t fb = full_even + stage * 8u;
           tma_load_2d_pair(sa, half ? o.a64 : o.a, fb, kc, t.a_row);
-          tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
+          if (half && t.kind == TASK_R1) {
+            // a split up/gate tile: this CTA's 128 weight rows are up rows 64 r .. 64 r + 63
+            // of the column tile, then the same gate rows, so each TMEM lane holds the up and
+            // the gate values of the same h columns
+            tma_load_2d_pair(sb, &maps.w_up64, fb, kc, o.b_row + 64 * walk.rank);
+            tma_load_2d_pair(sb + PAIR_B_STAGE_BYTES / 2, &maps.w_gate64, fb, kc, o.b_row + 64 * walk.rank);
+          } else {
+            tma_load_2d_pair(sb, bmap_pair, fb, kc, brow_pair);
+          }
           if constexpr (kMxPair) {
             if (mx) {  // scale blocks: this CTA's A rows, then all 256 B rows (two blocks)
               uint8_t* ssf2 = sf_slots + stage * SF_STAGE_BYTES;
@@ -1305,6 +1352,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * ACC_COLS;
         const int r0 = q * 32;                        // the warp's first tile row
         int nrows = min(32, max(0, t.rows - r0));  // its valid rows
+        bool store_ok = true;                      // (debug builds: false when a bounds check failed)
 #ifdef MOE_DEBUG_LOG
         {
           const bool col_ok = (tmem & 0xFFFFu) + acc * ACC_COLS + ACC_COLS <= (uint32_t)TMEM_COLS;
@@ -1317,25 +1365,39 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
                       y_offset(p, jj / p.k, jj % p.k, t.n) + BN_DOWN <= (size_t)p.n_chunks * BM * p.kY * p.D;
           }
           if (!DBG_CHECK(p, col_ok, 20, tmem, acc, ti) || !DBG_CHECK(p, rows_ok, 21 + t.kind, t.out_row, r0, ti))
-            nrows = 0;
+            nrows = 0, store_ok = false;
         }
 #endif
-        EpiStage& st = epi[q];
         const AccRelease rel{&tempty[acc], tempty_even + acc * 8u, &thead[acc], thead_even + acc * 8u, kPair};
-        const bool split = kPair && !kMxPair && t.half;  // a routed tile split over the pair
-        if (split && t.kind == TASK_R1) {
-          // lanes 32 (q % 2) + lane of the CTA's 64 rows; gate values in the warp of quadrant q % 2 + 2
-          const int hq = q & 1;
-          epilogue_swiglu_split(taddr, st, epi[hq + 2],
-                                p.ring_h + (size_t)(t.out_row + 32 * hq) * p.I + t.n * BN_UP, p.I,
-                                min(32, max(0, t.rows - 32 * hq)), rel, q >= 2, 3 + hq);
-        } else if (split) {  // TASK_R2: lanes 0-63 output columns 0-127, lanes 64-127 columns 128-255
+        if constexpr (G::kDirectEpi) {
+          // a routed tile split over the pair (one M = 128 MMA): each CTA's 64 rows sit in
+          // TMEM lanes 0-63 and again in lanes 64-127; lanes 0-63 hold output columns 0-127
+          // (split up/gate tiles: h columns 0-63, up then gate), lanes 64-127 the rest
           const int hq = q & 1, hrow = 32 * hq + lane;
-          const int j = hrow < t.rows ? p.sched[(size_t)(t.p0 + hrow) * 3 + 2] : 0;
-          epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, j / p.k, j % p.k, t.n),
-                                   min(32, max(0, t.rows - 32 * hq)), rel, p.status + 1, BN_DOWN / 2,
-                                   (q >> 1) * (BN_DOWN / 2));
-        } else if (t.kind == TASK_R1 && p.mx) {
+          if (t.kind == TASK_R1 && t.half) {
+            epilogue_swiglu_direct(taddr, p.ring_h + (size_t)(t.out_row + hrow) * p.I + t.n * BN_UP + (q >> 1) * 64,
+                                   store_ok && hrow < t.rows, rel, 64, 64);
+          } else if (t.kind == TASK_R1) {
+            epilogue_swiglu_direct(taddr, p.ring_h + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
+                                   store_ok && row < t.rows, rel, BN_UP, BN_UP);
+          } else if (t.kind == TASK_S1) {
+            epilogue_swiglu_direct(taddr, p.h_s + (size_t)(t.out_row + row) * p.I_s + t.n * BN_UP,
+                                   store_ok && row < t.rows, rel, BN_UP, BN_UP);
+          } else if (t.kind == TASK_R2 && t.half) {
+            const int j = hrow < t.rows ? p.sched[(size_t)(t.p0 + hrow) * 3 + 2] : 0;
+            epilogue_copy_f16_direct(taddr, p.Y + y_offset(p, j / p.k, j % p.k, t.n) + (q >> 1) * (BN_DOWN / 2),
+                                     store_ok && hrow < t.rows, rel, p.status + 1, BN_DOWN / 2);
+          } else if (t.kind == TASK_R2) {
+            const int j = row < t.rows ? p.sched[(size_t)(t.p0 + row) * 3 + 2] : 0;
+            epilogue_copy_f16_direct(taddr, p.Y + y_offset(p, j / p.k, j % p.k, t.n), store_ok && row < t.rows, rel,
+                                     p.status + 1, BN_DOWN);
+          } else {  // the shared expert's output: staging slot k of its tokens
+            epilogue_copy_f16_direct(taddr, p.Y + y_offset(p, t.out_row + row, p.k, t.n), store_ok && row < t.rows,
+                                     rel, p.status + 1, BN_DOWN);
+          }
+        } else {
+        EpiStage& st = epi[q];
+        if (t.kind == TASK_R1 && p.mx) {
           epilogue_swiglu_mx(taddr, reinterpret_cast<uint8_t*>(p.ring_h) + (size_t)(t.out_row + row) * p.I + t.n * BN_UP,
                              p.sfh + ((size_t)t.mt * (p.I / BK_MX) + t.n) * SF_BLOCK_BYTES, row, row < t.rows, rel);
         } else if (t.kind == TASK_R1) {
@@ -1349,6 +1411,7 @@ __device__ __forceinline__ void mega_body(const TensorMaps& maps, const FwdParam
         } else {  // the shared expert's output: staging slot k of its tokens
           epilogue_copy_f16_staged(taddr, st, p.Y, (long long)y_offset(p, t.out_row + row, p.k, t.n), nrows, rel,
                                    p.status + 1);
+        }
         }
         // h tiles are read back by TMA (async proxy); Y and out only by plain loads
         if (t.kind == TASK_R1 || t.kind == TASK_S1) fence_proxy_async_global();
