@@ -11,7 +11,7 @@ fp64 oracle.  The one-CTA kernel is used (ring and spread dispatch).
 
 The fp16 staging rows saturate at +-65504: a layer whose expert outputs leave
 that range must say so through MOE_STATUS_STAGING_OVERFLOW rather than return
-MOE_STATUS_OK with a wrong result.
+MOE_STATUS_OK with a wrong result, with one CTA per tile and with CTA pairs.
 """
 import time
 
@@ -61,13 +61,15 @@ def test_wait_that_runs_out_reports_timeout_and_the_workspace_recovers(dispatch)
     gpu_util.check_out(gpu_util.bf16_dev_to_f64(res["out"]), ref)
 
 
-def test_staging_overflow_is_reported():
+@pytest.mark.parametrize("mma_pair", [0, 1])
+def test_staging_overflow_is_reported(mma_pair):
+    # one CTA per tile (staged epilogue stores) and CTA pairs (rows stored from registers)
     import gpu_util
     import routing_grouped_expert_gemm_gb300 as rg
 
     shape = mi.custom_shape(256, 256, 128, 16, 4, 128, config_id=320)
     inp = mi.make_inputs(shape, calibration={"beta": None, "redraw": {}})
-    layer = gpu_util.Layer(inp, minibatch=512, ring_slots=2, gather_ctas=2)
+    layer = gpu_util.Layer(inp, minibatch=512, ring_slots=2, gather_ctas=2, mma_pair=mma_pair)
     x = gpu_util.to_dev_bf16(inp.x)
     assert layer.run(x)["status"] == rg.MOE_STATUS_OK
     # expert outputs ~N(0, 1) scaled by 2^17: far outside the fp16 range of the staging rows
